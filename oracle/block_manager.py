@@ -1,0 +1,144 @@
+"""Block manager model: free-block FIFO, ref_cnt, block tables — test infrastructure only.
+
+Sources:
+
+* "PagedAttention: manage the KV cache like virtual memory", §3.2: the pool keeps a
+  free-block queue; allocation pops from its head and freeing pushes to its tail;
+  every block carries a reference count.  §3.3: admission pops enough free blocks for
+  the prompt; each decode token fills the current last block and a full block makes
+  the sequence pop one more; finishing decrements every block's count and a block is
+  really freed when its count reaches 0.  §2/§3.5: a block is free (count 0) or owned
+  (count > 0).  §4: admission succeeds while enough free blocks remain.
+* "Lecture 33 — KV Cache management", §2.2 (per-sequence block table, slot address)
+  and §2.4 (fork copies only the table and raises each block's count; a write into a
+  block whose count is above 1 first takes a new block, copies the old block into
+  it, points the writer's table at it and lowers the old block's count).
+
+Readings where the pages are silent:
+
+* A sequence's blocks are released in table order when it is freed.
+* ``import_seq`` claims named blocks directly (used to set up synthetic states such
+  as two sequences sharing a block); a claimed free block leaves the free queue.
+* Running out of free blocks raises ``NoBlocks`` and leaves the state unchanged.
+"""
+from __future__ import annotations
+
+from collections import deque
+from typing import Dict, List, Optional, Sequence, Tuple
+
+
+class BlockManagerError(Exception):
+    pass
+
+
+class NoBlocks(BlockManagerError):
+    pass
+
+
+class InvalidArg(BlockManagerError):
+    pass
+
+
+class BlockManagerModel:
+    def __init__(self, num_blocks: int, block_size: int):
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.free_queue = deque(range(num_blocks))   # head = next to allocate
+        self.ref_cnt = [0] * num_blocks
+        self.tables: Dict[int, List[int]] = {}
+        self.num_tokens: Dict[int, int] = {}
+
+    # -- pool ---------------------------------------------------------------------------
+    def num_free(self) -> int:
+        return len(self.free_queue)
+
+    def _pop(self) -> int:
+        if not self.free_queue:
+            raise NoBlocks("free block queue is empty")
+        b = self.free_queue.popleft()
+        assert self.ref_cnt[b] == 0
+        self.ref_cnt[b] = 1
+        return b
+
+    def _release(self, b: int) -> None:
+        assert self.ref_cnt[b] > 0
+        self.ref_cnt[b] -= 1
+        if self.ref_cnt[b] == 0:
+            self.free_queue.append(b)
+
+    # -- sequences ----------------------------------------------------------------------
+    def import_seq(self, seq: int, blocks: Sequence[int], n_tokens: int) -> None:
+        if seq in self.tables:
+            raise InvalidArg("sequence exists")
+        if len(blocks) != -(-n_tokens // self.block_size):
+            raise InvalidArg("block count does not cover n_tokens")
+        for b in blocks:
+            if not 0 <= b < self.num_blocks:
+                raise InvalidArg("block id out of range")
+        for b in blocks:
+            if self.ref_cnt[b] == 0:
+                self.free_queue.remove(b)
+            self.ref_cnt[b] += 1
+        self.tables[seq] = list(blocks)
+        self.num_tokens[seq] = n_tokens
+
+    def allocate(self, seq: int, n_tokens: int) -> None:
+        """Admit a sequence with an ``n_tokens`` prompt: pop ceil(n / B) blocks."""
+        if seq in self.tables:
+            raise InvalidArg("sequence exists")
+        need = -(-n_tokens // self.block_size)
+        if need > len(self.free_queue):
+            raise NoBlocks("not enough free blocks")
+        self.tables[seq] = [self._pop() for _ in range(need)]
+        self.num_tokens[seq] = n_tokens
+
+    def append_slot(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
+        """Reserve the slot of the sequence's next token; returns (slot, cow_pair or None)."""
+        table = self.tables[seq]
+        p = self.num_tokens[seq]
+        bs = self.block_size
+        cow = None
+        if p % bs == 0:                      # last block full (or none yet): grow by one block
+            table.append(self._pop())
+        else:
+            last = table[p // bs]
+            if self.ref_cnt[last] > 1:       # shared: copy-on-write before the write
+                new = self._pop()
+                self.ref_cnt[last] -= 1
+                table[p // bs] = new
+                cow = (last, new)
+        self.num_tokens[seq] = p + 1
+        return table[p // bs] * bs + p % bs, cow
+
+    def append_slots(self, seq: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
+        slots, cows = [], []
+        for _ in range(n):
+            s, c = self.append_slot(seq)
+            slots.append(s)
+            if c is not None:
+                cows.append(c)
+        return slots, cows
+
+    def fork(self, parent: int, child: int) -> None:
+        if child in self.tables:
+            raise InvalidArg("sequence exists")
+        self.tables[child] = list(self.tables[parent])
+        self.num_tokens[child] = self.num_tokens[parent]
+        for b in self.tables[child]:
+            self.ref_cnt[b] += 1
+
+    def free(self, seq: int) -> None:
+        for b in self.tables.pop(seq):
+            self._release(b)
+        del self.num_tokens[seq]
+
+    def export(self, seqs: Sequence[int], max_blocks: int) -> Tuple[List[List[int]], List[int]]:
+        """Block tables padded with -1 to ``max_blocks`` and the token counts."""
+        tables, lens = [], []
+        for s in seqs:
+            t = self.tables[s]
+            if len(t) > max_blocks:
+                raise InvalidArg("table longer than max_blocks")
+            tables.append(t + [-1] * (max_blocks - len(t)))
+            lens.append(self.num_tokens[s])
+        return tables, lens
