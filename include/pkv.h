@@ -1,0 +1,245 @@
+/*
+ * pkv.h — C ABI of libpkv: attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * The method: a sequence's K/V rows live in fixed-size physical blocks of one pool
+ * tensor, found through a per-sequence block table (logical block -> physical block),
+ * as in "Lecture 33 — KV Cache management: PagedAttention, Continuous Batching,
+ * Chunked Prefill", §2.2; attention kernels read the blocks in place (§2.3); shared
+ * blocks are split by copy-on-write (§2.4); a prefill chunk attends its cached
+ * history causally (§4.2).  The host block manager follows "PagedAttention: manage
+ * the KV cache like virtual memory", §3.2–§3.3.
+ *
+ * Conventions for every device call below
+ *   - Pointers marked (device) are device pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  All tensors are dense, row-major, with
+ *     the layouts given per argument, and 16-byte aligned.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default stream).
+ *     Argument checks run on the host before anything is enqueued; a failed check
+ *     returns PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED and enqueues nothing.
+ *     A launch failure returns PKV_ERR_CUDA.
+ *   - Data-dependent faults the host cannot see (a block id outside the pool, a slot
+ *     outside the pool, a context_len beyond the block table, a copy pair that chains)
+ *     never fault the GPU: the kernel skips the access and sets a bit in the library's
+ *     device error word, read with pkv_get_device_error().
+ *   - No call aborts, traps, prints or spins without bound.
+ *
+ * KV cache layout (both K and V): [num_blocks][num_kv_heads][block_size][head_dim]
+ * of kv_dtype.  Slot s addresses token row s % block_size of physical block
+ * s / block_size (Lecture 33 §2.2: base + block * block_stride + offset * token_stride).
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* a host-visible argument is out of range / misaligned */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid, but this build has no kernel for it (e.g. head_dim 96) */
+  PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pkv_decode_workspace_bytes() */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  PKV_ERR_NO_BLOCKS = 5,     /* block manager: the free-block queue cannot cover the request */
+  PKV_ERR_DEVICE_CHECK = 6   /* pkv_get_device_error() found a device-side check bit set */
+} pkv_status;
+
+typedef enum {
+  PKV_F16 = 0,
+  PKV_BF16 = 1,
+  PKV_FP8_E4M3 = 2           /* e4m3 "fn": bias 7, max 448, no inf; value = code * scale[kv_head] */
+} pkv_dtype;
+
+/* Device error word bits (pkv_get_device_error). */
+enum {
+  PKV_DEVERR_BLOCK_ID = 1u << 0,      /* a block table entry was outside [0, num_blocks) */
+  PKV_DEVERR_CONTEXT_LEN = 1u << 1,   /* context_len < 0, > max_blocks_per_seq * block_size or > max_context_len */
+  PKV_DEVERR_SLOT = 1u << 2,          /* a slot was >= num_blocks * block_size */
+  PKV_DEVERR_COPY_PAIR = 1u << 3,     /* a copy pair was out of range or its dst is also a src */
+  PKV_DEVERR_TIMEOUT = 1u << 4,       /* a bounded wait on an async copy / MMA gave up */
+  PKV_DEVERR_CHUNK = 1u << 5          /* a prefill chunk's cu_q_lens / q_start_pos were inconsistent */
+};
+
+/* The paged pool (Lecture 33 §2.2, "physical KV block pool"): K and V are two such tensors. */
+typedef struct {
+  int num_blocks;            /* physical blocks in the pool */
+  int num_kv_heads;
+  int block_size;            /* tokens per block; 16 */
+  int head_dim;              /* 64 or 128 */
+  pkv_dtype kv_dtype;
+  const float* k_scale;      /* (device) [num_kv_heads] fp32, e4m3 caches only, else NULL */
+  const float* v_scale;      /* (device) [num_kv_heads] fp32, e4m3 caches only, else NULL */
+} pkv_cache_desc;
+
+PKV_API const char* pkv_status_string(pkv_status s);
+PKV_API int pkv_version(void);       /* (major << 16) | minor */
+
+/*
+ * kv_write ("reshape_and_cache").  "PagedAttention: manage the KV cache like virtual
+ * memory" §3.3: each new token fills its sequence's current last block; Lecture 33
+ * §4.2: a prefill chunk's K/V is written into the cache too.
+ *   k_new, v_new   (device) [num_tokens][num_kv_heads][head_dim] of in_dtype
+ *   slot_mapping   (device) int64 [num_tokens]; slot < 0 = padding token, skipped
+ *   k_cache/v_cache (device) pool tensors described by `cache`
+ * For every token t with slot s >= 0 and every kv head h:
+ *   k_cache[s / B][h][s % B][:] = k_new[t][h][:]   (same for V)
+ * in_dtype == kv_dtype copies bytes.  in_dtype f16/bf16 into an e4m3 cache quantises
+ * x / scale[h] (fp32 divide) to e4m3, round-to-nearest-even, saturating at ±448.
+ * Slots that repeat within one call: one of the writers wins (unspecified which).
+ */
+PKV_API pkv_status pkv_kv_write(const void* k_new, const void* v_new, pkv_dtype in_dtype, int num_tokens,
+                        const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                        const pkv_cache_desc* cache, pkv_stream_t stream);
+
+/*
+ * copy_blocks: the copy step of copy-on-write (Lecture 33 §2.4: the writer gets a new
+ * block holding a copy of the shared block).
+ *   block_pairs (device) int32 [num_pairs][2] = (src, dst)
+ * For each pair, the whole block dst of K and of V (all kv heads, all rows) becomes a
+ * copy of block src.  No dst may also appear as a src or twice as a dst (the result
+ * would depend on order): such pairs, and ids outside the pool, are skipped and flagged
+ * PKV_DEVERR_COPY_PAIR.
+ */
+PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                           const int32_t* block_pairs, int num_pairs, pkv_stream_t stream);
+
+/*
+ * Workspace bytes pkv_paged_decode needs on the current device (split-KV partials and
+ * per-(sequence, kv head) merge counters).  partition_size = 0 selects the balanced
+ * split (work cut evenly over all SMs); > 0 cuts every sequence into partitions of that
+ * many tokens (a multiple of block_size).  Zero the workspace once after allocating it;
+ * every decode call leaves its counters at zero again.
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_context_len, int partition_size);
+
+/*
+ * paged_decode: one query token per running sequence (Lecture 33 §2.3).  For sequence
+ * i, query head h and kv head g = h / (num_heads / num_kv_heads), with L = context_lens[i]:
+ *   s_j = scale * q[i][h] . K_i[j]  for j < L, where K_i[j] = k_cache[T_i[j / B]][g][j % B]
+ *   out[i][h] = sum_j softmax(s)_j V_i[j]                         (zeros when L == 0)
+ * with T_i = block_tables[i].  Computed as an online softmax per KV split followed by a
+ * log-sum-exp merge of the splits, fp32 accumulation.
+ *   out            (device) [num_seqs][num_heads][head_dim] of q_dtype
+ *   q              (device) [num_seqs][num_heads][head_dim] of q_dtype (f16 or bf16)
+ *   block_tables   (device) int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   (device) int32 [num_seqs]; tokens to attend, including any token
+ *                  written this step
+ *   max_context_len host upper bound of context_lens (sizes the partitioned workspace)
+ *   partition_size  0 = balanced split; else tokens per partition (multiple of block_size)
+ *   workspace       (device) >= pkv_decode_workspace_bytes(...) bytes, zeroed once
+ * Supported: kv f16/bf16 with the same q dtype, or e4m3 kv with f16/bf16 q (the e4m3
+ * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16;
+ * num_heads / num_kv_heads in 1..8.
+ */
+PKV_API pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                            const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context_len, float scale,
+                            int partition_size, void* workspace, size_t workspace_bytes,
+                            pkv_stream_t stream);
+
+/*
+ * paged_prefill_chunk: causal attention of prefill chunks over their paged history
+ * (Lecture 33 §4.2: a chunk attends the earlier chunks' cached KV, masked causally).
+ * Chunk c holds query rows cu_q_lens[c] .. cu_q_lens[c+1]-1; row r of the chunk is at
+ * absolute position p = q_start_pos[c] + r of sequence c and attends that sequence's
+ * keys 0..p (its cached history and itself).  The chunk's own K/V must already be in the
+ * cache (pkv_kv_write first).
+ *   out, q        (device) [total_q][num_heads][head_dim] of q_dtype (bf16 or f16; same as kv)
+ *   cu_q_lens     (device) int32 [num_chunks + 1], cu_q_lens[0] = 0, cu_q_lens[num_chunks] = total_q
+ *   q_start_pos   (device) int32 [num_chunks]
+ *   block_tables  (device) int32 [num_chunks][max_blocks_per_seq]
+ *   max_q_len     host upper bound of the chunks' lengths (sizes the grid)
+ * Supported: f16/bf16 cache with the same q dtype, head_dim 128, block_size 16,
+ * num_heads / num_kv_heads in 1..8.  Tensor cores (tcgen05, TMEM accumulators), K/V
+ * tiles fetched by TMA straight from the physical blocks.
+ */
+PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
+                                   const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                                   int num_chunks, int total_q, int max_q_len, int num_heads,
+                                   const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq, float scale,
+                                   pkv_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads and clears the library's device error word on the
+ * current device.  *code receives the PKV_DEVERR_* bits (0 = clean).  Returns
+ * PKV_ERR_DEVICE_CHECK when any bit was set, PKV_OK otherwise.
+ */
+PKV_API pkv_status pkv_get_device_error(int* code, pkv_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Host block manager ("PagedAttention: manage the KV cache like virtual memory" §3.2–§3.3;
+ * Lecture 33 §2.2, §2.4).  A FIFO free-block queue (allocate pops the head, free pushes
+ * the tail), a ref_cnt per block, and one block table per sequence.  It produces the
+ * block tables, context lengths, slot mappings and copy-on-write pairs the device calls
+ * consume.  Host memory only; not thread-safe (one manager per scheduler thread).
+ * Every call that fails leaves the manager unchanged.
+ * ------------------------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A pool of num_blocks blocks of block_size tokens; the free queue starts as 0..num_blocks-1. */
+PKV_API pkv_status pkv_bm_create(int num_blocks, int block_size, pkv_block_manager** out);
+PKV_API void pkv_bm_destroy(pkv_block_manager* bm);
+
+/* Claim the listed blocks for a new sequence holding n_tokens tokens (n_blocks must equal
+ * ceil(n_tokens / block_size)); each block's ref_cnt rises by one and a free block leaves
+ * the free queue.  Used to set up states such as shared prefixes. */
+PKV_API pkv_status pkv_bm_import_seq(pkv_block_manager* bm, int64_t seq, const int32_t* blocks,
+                             int n_blocks, int n_tokens);
+
+/* Admit a sequence with an n_tokens prompt: pop ceil(n_tokens / block_size) blocks. */
+PKV_API pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq, int n_tokens);
+
+/* Reserve the slot of the sequence's next token.  If the token starts a new block, one
+ * block is popped.  If it lands in a block whose ref_cnt > 1, copy-on-write: a new block
+ * is popped, (*cow_src, *cow_dst) = (old, new), the table points at the new block and the
+ * old block's ref_cnt drops by one; otherwise both are set to -1. */
+PKV_API pkv_status pkv_bm_append_slot(pkv_block_manager* bm, int64_t seq, int64_t* slot,
+                              int32_t* cow_src, int32_t* cow_dst);
+
+/* One decode step for a batch: append_slot for seqs[0..n) in order, then export.
+ *   slot_mapping  int64 [n]; cow_pairs int32 [n][2] (first *n_cow rows used)
+ *   tables        int32 [n][max_blocks] padded with -1; lens int32 [n] (after the step)
+ * Fails with PKV_ERR_NO_BLOCKS, changing nothing, if the free queue cannot cover it. */
+PKV_API pkv_status pkv_bm_step_decode(pkv_block_manager* bm, const int64_t* seqs, int n, int max_blocks,
+                              int64_t* slot_mapping, int32_t* cow_pairs, int* n_cow,
+                              int32_t* tables, int32_t* lens);
+
+/* Reserve n consecutive slots (a prefill chunk); slots int64 [n], cow_pairs int32 [n][2]. */
+PKV_API pkv_status pkv_bm_append_slots(pkv_block_manager* bm, int64_t seq, int n, int64_t* slots,
+                               int32_t* cow_pairs, int* n_cow);
+
+/* child's table becomes a copy of parent's; every block's ref_cnt rises by one. */
+PKV_API pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
+
+/* Drop the sequence: each block's ref_cnt falls by one; blocks reaching 0 go to the
+ * tail of the free queue, in table order. */
+PKV_API pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq);
+
+/* tables int32 [n][max_blocks] (padded with -1), lens int32 [n]. */
+PKV_API pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n, int max_blocks,
+                         int32_t* tables, int32_t* lens);
+
+PKV_API int pkv_bm_ref_cnt(const pkv_block_manager* bm, int block);      /* -1 if out of range */
+PKV_API int pkv_bm_num_free(const pkv_block_manager* bm);
+/* The free queue from head to tail into out[0..max_n); returns the queue length. */
+PKV_API int pkv_bm_free_queue(const pkv_block_manager* bm, int32_t* out, int max_n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

@@ -111,12 +111,19 @@ class BlockManagerModel:
         return table[p // bs] * bs + p % bs, cow
 
     def append_slots(self, seq: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
+        """``n`` consecutive append_slot calls; all of them or none (state restored on NoBlocks)."""
+        saved = (deque(self.free_queue), list(self.ref_cnt), {k: list(v) for k, v in self.tables.items()},
+                 dict(self.num_tokens))
         slots, cows = [], []
-        for _ in range(n):
-            s, c = self.append_slot(seq)
-            slots.append(s)
-            if c is not None:
-                cows.append(c)
+        try:
+            for _ in range(n):
+                s, c = self.append_slot(seq)
+                slots.append(s)
+                if c is not None:
+                    cows.append(c)
+        except NoBlocks:
+            self.free_queue, self.ref_cnt, self.tables, self.num_tokens = saved
+            raise
         return slots, cows
 
     def fork(self, parent: int, child: int) -> None:

@@ -1,0 +1,275 @@
+// Host block manager: the free-block queue, per-block ref_cnt and per-sequence block
+// tables of "PagedAttention: manage the KV cache like virtual memory" §3.2–§3.3, with
+// fork and copy-on-write from "Lecture 33 — KV Cache management" §2.4.
+//
+// The free queue is an intrusive doubly linked list over block ids (allocate pops the
+// head, free pushes the tail, a claimed block is unlinked from the middle in O(1)).
+// Every entry point validates first and mutates after, so a failing call leaves the
+// manager unchanged.
+#include <cstdint>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "pkv.h"
+
+namespace {
+
+struct Seq {
+  std::vector<int32_t> blocks;
+  int64_t n_tokens = 0;
+};
+
+}  // namespace
+
+struct pkv_block_manager {
+  int num_blocks = 0;
+  int block_size = 0;
+  std::vector<int32_t> ref;
+  std::vector<int32_t> prev, next;   // free-list links; -1 = none
+  std::vector<uint8_t> in_free;
+  int32_t head = -1, tail = -1;
+  int num_free = 0;
+  std::unordered_map<int64_t, Seq> seqs;
+
+  void push_tail(int32_t b) {
+    prev[b] = tail;
+    next[b] = -1;
+    if (tail >= 0) next[tail] = b; else head = b;
+    tail = b;
+    in_free[b] = 1;
+    ++num_free;
+  }
+  void unlink(int32_t b) {
+    if (prev[b] >= 0) next[prev[b]] = next[b]; else head = next[b];
+    if (next[b] >= 0) prev[next[b]] = prev[b]; else tail = prev[b];
+    prev[b] = next[b] = -1;
+    in_free[b] = 0;
+    --num_free;
+  }
+  int32_t pop_head() {  // caller checked num_free > 0
+    int32_t b = head;
+    unlink(b);
+    ref[b] = 1;
+    return b;
+  }
+  void release(int32_t b) {
+    if (--ref[b] == 0) push_tail(b);
+  }
+  int64_t blocks_for(int64_t n_tokens) const { return (n_tokens + block_size - 1) / block_size; }
+
+  // Blocks one append_slot on `s` would pop (0 or 1), given extra ref drops in `drop`.
+  int pops_for_append(const Seq& s, int64_t n_tokens, const std::unordered_map<int32_t, int>* drop) const {
+    if (n_tokens % block_size == 0) return 1;
+    int32_t last = s.blocks[n_tokens / block_size];
+    int r = ref[last];
+    if (drop) {
+      auto it = drop->find(last);
+      if (it != drop->end()) r -= it->second;
+    }
+    return r > 1 ? 1 : 0;
+  }
+
+  // Appends one token; the caller guaranteed a free block when one is needed.
+  int64_t append(Seq& s, int32_t* cow_src, int32_t* cow_dst) {
+    const int64_t p = s.n_tokens;
+    *cow_src = -1;
+    *cow_dst = -1;
+    if (p % block_size == 0) {
+      s.blocks.push_back(pop_head());
+    } else {
+      int32_t& last = s.blocks[p / block_size];
+      if (ref[last] > 1) {
+        int32_t fresh = pop_head();
+        --ref[last];
+        *cow_src = last;
+        *cow_dst = fresh;
+        last = fresh;
+      }
+    }
+    s.n_tokens = p + 1;
+    return int64_t(s.blocks[p / block_size]) * block_size + p % block_size;
+  }
+};
+
+extern "C" {
+
+pkv_status pkv_bm_create(int num_blocks, int block_size, pkv_block_manager** out) {
+  if (!out || num_blocks <= 0 || block_size <= 0) return PKV_ERR_INVALID_ARG;
+  auto* bm = new (std::nothrow) pkv_block_manager();
+  if (!bm) return PKV_ERR_INVALID_ARG;
+  bm->num_blocks = num_blocks;
+  bm->block_size = block_size;
+  bm->ref.assign(num_blocks, 0);
+  bm->prev.assign(num_blocks, -1);
+  bm->next.assign(num_blocks, -1);
+  bm->in_free.assign(num_blocks, 0);
+  for (int b = 0; b < num_blocks; ++b) bm->push_tail(b);
+  *out = bm;
+  return PKV_OK;
+}
+
+void pkv_bm_destroy(pkv_block_manager* bm) { delete bm; }
+
+pkv_status pkv_bm_import_seq(pkv_block_manager* bm, int64_t seq, const int32_t* blocks, int n_blocks,
+                             int n_tokens) {
+  if (!bm || n_tokens < 0 || n_blocks < 0 || (n_blocks > 0 && !blocks)) return PKV_ERR_INVALID_ARG;
+  if (bm->seqs.count(seq)) return PKV_ERR_INVALID_ARG;
+  if (bm->blocks_for(n_tokens) != n_blocks) return PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n_blocks; ++i)
+    if (blocks[i] < 0 || blocks[i] >= bm->num_blocks) return PKV_ERR_INVALID_ARG;
+  Seq s;
+  s.blocks.assign(blocks, blocks + n_blocks);
+  s.n_tokens = n_tokens;
+  for (int32_t b : s.blocks) {
+    if (bm->in_free[b]) bm->unlink(b);
+    ++bm->ref[b];
+  }
+  bm->seqs.emplace(seq, std::move(s));
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq, int n_tokens) {
+  if (!bm || n_tokens < 0 || bm->seqs.count(seq)) return PKV_ERR_INVALID_ARG;
+  int64_t need = bm->blocks_for(n_tokens);
+  if (need > bm->num_free) return PKV_ERR_NO_BLOCKS;
+  Seq s;
+  s.n_tokens = n_tokens;
+  for (int64_t i = 0; i < need; ++i) s.blocks.push_back(bm->pop_head());
+  bm->seqs.emplace(seq, std::move(s));
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_append_slot(pkv_block_manager* bm, int64_t seq, int64_t* slot, int32_t* cow_src,
+                              int32_t* cow_dst) {
+  if (!bm || !slot || !cow_src || !cow_dst) return PKV_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
+  if (bm->pops_for_append(it->second, it->second.n_tokens, nullptr) > bm->num_free) return PKV_ERR_NO_BLOCKS;
+  *slot = bm->append(it->second, cow_src, cow_dst);
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_append_slots(pkv_block_manager* bm, int64_t seq, int n, int64_t* slots, int32_t* cow_pairs,
+                               int* n_cow) {
+  if (!bm || n < 0 || (n > 0 && (!slots || !cow_pairs)) || !n_cow) return PKV_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
+  Seq& s = it->second;
+  // Pops needed: a copy-on-write of the current last block (if shared and partially
+  // filled) plus one block per block boundary crossed.
+  int64_t need = 0;
+  if (n > 0) {
+    need += bm->pops_for_append(s, s.n_tokens, nullptr) && (s.n_tokens % bm->block_size != 0) ? 1 : 0;
+    int64_t first_new = bm->blocks_for(s.n_tokens);
+    int64_t last_needed = bm->blocks_for(s.n_tokens + n);
+    need += last_needed - first_new;
+  }
+  if (need > bm->num_free) return PKV_ERR_NO_BLOCKS;
+  int nc = 0;
+  for (int i = 0; i < n; ++i) {
+    int32_t cs, cd;
+    slots[i] = bm->append(s, &cs, &cd);
+    if (cs >= 0) {
+      cow_pairs[2 * nc] = cs;
+      cow_pairs[2 * nc + 1] = cd;
+      ++nc;
+    }
+  }
+  *n_cow = nc;
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_step_decode(pkv_block_manager* bm, const int64_t* seqs, int n, int max_blocks,
+                              int64_t* slot_mapping, int32_t* cow_pairs, int* n_cow, int32_t* tables,
+                              int32_t* lens) {
+  if (!bm || n < 0 || max_blocks < 0 || !n_cow) return PKV_ERR_INVALID_ARG;
+  if (n > 0 && (!seqs || !slot_mapping || !cow_pairs || !tables || !lens)) return PKV_ERR_INVALID_ARG;
+  // Validate and count pops before changing anything.  A shared block copied by one
+  // sequence of the batch may no longer be shared when a later sequence reaches it.
+  std::unordered_set<int64_t> seen;
+  std::unordered_map<int32_t, int> drop;
+  int64_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seqs[i]);
+    if (it == bm->seqs.end() || !seen.insert(seqs[i]).second) return PKV_ERR_INVALID_ARG;
+    const Seq& s = it->second;
+    if (bm->blocks_for(s.n_tokens + 1) > max_blocks) return PKV_ERR_INVALID_ARG;
+    int pops = bm->pops_for_append(s, s.n_tokens, &drop);
+    if (pops && s.n_tokens % bm->block_size != 0) ++drop[s.blocks[s.n_tokens / bm->block_size]];
+    need += pops;
+  }
+  if (need > bm->num_free) return PKV_ERR_NO_BLOCKS;
+  int nc = 0;
+  for (int i = 0; i < n; ++i) {
+    Seq& s = bm->seqs[seqs[i]];
+    int32_t cs, cd;
+    slot_mapping[i] = bm->append(s, &cs, &cd);
+    if (cs >= 0) {
+      cow_pairs[2 * nc] = cs;
+      cow_pairs[2 * nc + 1] = cd;
+      ++nc;
+    }
+  }
+  *n_cow = nc;
+  return pkv_bm_export(bm, seqs, n, max_blocks, tables, lens);
+}
+
+pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child) {
+  if (!bm) return PKV_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(parent);
+  if (it == bm->seqs.end() || bm->seqs.count(child)) return PKV_ERR_INVALID_ARG;
+  Seq c = it->second;
+  for (int32_t b : c.blocks) ++bm->ref[b];
+  bm->seqs.emplace(child, std::move(c));
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq) {
+  if (!bm) return PKV_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
+  for (int32_t b : it->second.blocks) bm->release(b);
+  bm->seqs.erase(it);
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n, int max_blocks,
+                         int32_t* tables, int32_t* lens) {
+  if (!bm || n < 0 || max_blocks < 0) return PKV_ERR_INVALID_ARG;
+  if (n > 0 && (!seqs || !tables || !lens)) return PKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seqs[i]);
+    if (it == bm->seqs.end() || int64_t(it->second.blocks.size()) > max_blocks) return PKV_ERR_INVALID_ARG;
+    if (it->second.n_tokens > INT32_MAX) return PKV_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n; ++i) {
+    const Seq& s = bm->seqs.at(seqs[i]);
+    int32_t* row = tables + int64_t(i) * max_blocks;
+    size_t k = 0;
+    for (; k < s.blocks.size(); ++k) row[k] = s.blocks[k];
+    for (; k < size_t(max_blocks); ++k) row[k] = -1;
+    lens[i] = int32_t(s.n_tokens);
+  }
+  return PKV_OK;
+}
+
+int pkv_bm_ref_cnt(const pkv_block_manager* bm, int block) {
+  if (!bm || block < 0 || block >= bm->num_blocks) return -1;
+  return bm->ref[block];
+}
+
+int pkv_bm_num_free(const pkv_block_manager* bm) { return bm ? bm->num_free : -1; }
+
+int pkv_bm_free_queue(const pkv_block_manager* bm, int32_t* out, int max_n) {
+  if (!bm) return -1;
+  int k = 0;
+  for (int32_t b = bm->head; b >= 0; b = bm->next[b]) {
+    if (out && k < max_n) out[k] = b;
+    ++k;
+  }
+  return k;
+}
+
+}  // extern "C"

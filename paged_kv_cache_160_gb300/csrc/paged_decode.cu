@@ -1,0 +1,707 @@
+// paged_decode: one query token per running sequence over its paged K/V.
+//
+// Method ("Lecture 33 — KV Cache management" §2.3): for each sequence and head, walk the
+// sequence's logical blocks, look up each physical block in the block table, load its
+// 16 K rows, form the scores with the query, keep a running (online) softmax, then load
+// the 16 V rows and accumulate; no gather copy is ever made.  The result equals plain
+// softmax attention (§8.1 row 1).  GQA: query head h reads kv head h / group
+// ("PagedAttention: manage the KV cache like virtual memory" §9 names GQA; the
+// contiguous grouping is this library's reading).
+//
+// GB300 design
+//   * Work unit = one (sequence, kv head, logical block) tile: 16 tokens x head_dim of K and
+//     of V, each a contiguous run in the [block][kv_head][row][dim] pool.
+//   * Persistent grid, one CTA per SM, 4 independent worker warps per CTA.  The flattened
+//     tile list (sequence-major, kv head, block) is cut into equal contiguous ranges, one
+//     per worker ("balanced" split), or into fixed partitions of partition_size tokens.
+//   * Each worker warp owns a ring of TMA stages: lane 0 issues 2-D tensor loads of the K
+//     and V tile (128-byte swizzled) straight from the physical block named by the block
+//     table, completing on an mbarrier; the warp waits, computes, and refills the stage.
+//   * All query heads of a kv head (group <= 8) are processed together on tensor cores:
+//     S^T[16 tok x 8 heads] = K[16 x D] * Q^T (m16n8k16, K as the A operand from ldmatrix),
+//     online softmax in registers (warp shuffles over the 16 tokens), P^T transposed with
+//     movmatrix, O^T[D x 8] += V^T[D x 16] * P^T (V^T via ldmatrix.trans).  For e4m3 caches
+//     the fragments are loaded with plain shared loads in a head_dim/token order chosen so
+//     every lane reads 16 contiguous bytes, and converted exactly to fp16.
+//   * A range that covers only part of a (sequence, kv head) writes a partial (m, l, o) to
+//     the workspace; the last arriving piece (atomic counter, no waiting) merges all pieces
+//     by log-sum-exp and resets the counter, so one launch does split + merge.
+#include <algorithm>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace {
+
+enum { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+
+constexpr int kBS = 16;        // tokens per block
+constexpr int kWarps = 4;      // worker warps per CTA
+constexpr int kStages = 4;     // TMA stages per worker warp
+constexpr int kMaxGroup = 8;   // query heads per kv head handled by one n=8 MMA tile
+
+template <int KV, int D>
+struct Cfg {
+  static constexpr int kElt = KV == KV_E4M3 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElt;
+  static constexpr int kNBox = kRowBytes / 128;       // 128-byte-wide TMA boxes per row
+  static constexpr int kBoxElems = 128 / kElt;
+  static constexpr int kTileBytes = kBS * kRowBytes;  // one 16-row K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kKSteps = D / 16;
+  static constexpr int kMTiles = D / 16;
+  static constexpr bool kBF16 = KV == KV_BF16;        // MMA input type (e4m3 computes in fp16)
+  static_assert(kRowBytes % 128 == 0, "rows must span whole 128-byte swizzle atoms");
+  static_assert(KV != KV_E4M3 || D == 128, "e4m3 path is written for head_dim 128");
+};
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const float* k_scale;
+  const float* v_scale;
+  int num_seqs;
+  int num_kv_heads;
+  int group;
+  int max_blocks;
+  int max_len;            // min(max_blocks * 16, max_context_len): lengths are clamped to it
+  int num_blocks;
+  int part_blocks;        // blocks per partition; 0 = balanced split
+  int num_workers;        // gridDim.x * kWarps
+  float scale_log2;       // softmax scale * log2(e)
+  int* counters;          // [num_seqs * num_kv_heads]
+  float2* ml;             // [slots][group] (running max in log2 units, sum of exponentials)
+  float* po;              // [slots][group][D] unnormalised partial outputs
+  unsigned* err;
+};
+
+struct Tile {
+  int s, h, b, nb, len;
+};
+
+// Largest s in [0, S) with mult * cum[s] <= t.
+__device__ __forceinline__ int find_seq(const int* cum, int S, int64_t t, int mult) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (int64_t(mult) * cum[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int clamp_len(int L, int max_len) { return min(max(L, 0), max_len); }
+
+template <int QT>
+__device__ __forceinline__ float2 q_pair(const void* q, int64_t elem) {
+  if constexpr (QT == KV_BF16) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(static_cast<const __nv_bfloat16*>(q) + elem));
+  } else {
+    return __half22float2(*reinterpret_cast<const __half2*>(static_cast<const __half*>(q) + elem));
+  }
+}
+
+template <int QT>
+__device__ __forceinline__ void store_out(void* out, int64_t elem, float v) {
+  if constexpr (QT == KV_BF16) {
+    static_cast<__nv_bfloat16*>(out)[elem] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(out)[elem] = __float2half_rn(v);
+  }
+}
+
+// head_dim index held by accumulator row `r` (0: row g, 1: row g + 8) of m-tile i.
+template <int KV>
+__device__ __forceinline__ int out_dim(int i, int r, int g) {
+  if constexpr (KV == KV_E4M3) return 16 * g + 2 * i + r;
+  else return 16 * i + g + 8 * r;
+}
+
+template <int KV, int QT, int D>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        const DecodeParams p) {
+  using C = Cfg<KV, D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+  __shared__ int warp_tot[kWarps * 2];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.num_seqs;
+  const int Hkv = p.num_kv_heads;
+  const int G = p.group;
+  const int PB = p.part_blocks;
+  int* cum_nb = reinterpret_cast<int*>(smem + kWarps * kStages * C::kStageBytes);   // [S + 1]
+  int* cum_np = cum_nb + (S + 1);                                                    // [S + 1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(&bars[warp][st], 1);
+    fence_mbar_init();
+  }
+
+  // ---- per-CTA prefix sums of blocks (and partitions) per sequence ---------------------
+  {
+    const int per = (S + blockDim.x - 1) / blockDim.x;
+    const int s0 = min(S, int(threadIdx.x) * per), s1 = min(S, s0 + per);
+    int a = 0, u = 0;
+    for (int s = s0; s < s1; ++s) {
+      const int L = p.context_lens[s];
+      const int Lc = clamp_len(L, p.max_len);
+      if (Lc != L) set_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+      const int nb = (Lc + kBS - 1) / kBS;
+      a += nb;
+      u += PB ? (nb + PB - 1) / PB : 0;
+    }
+    int ia = a, iu = u;   // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int va = __shfl_up_sync(0xffffffffu, ia, o), vu = __shfl_up_sync(0xffffffffu, iu, o);
+      if (lane >= o) { ia += va; iu += vu; }
+    }
+    if (lane == 31) { warp_tot[warp] = ia; warp_tot[kWarps + warp] = iu; }
+    __syncthreads();
+    int ba = 0, bu = 0;
+    for (int w = 0; w < warp; ++w) { ba += warp_tot[w]; bu += warp_tot[kWarps + w]; }
+    int ra = ba + ia - a, ru = bu + iu - u;   // exclusive prefix at s0
+    for (int s = s0; s < s1; ++s) {
+      const int nb = (clamp_len(p.context_lens[s], p.max_len) + kBS - 1) / kBS;
+      cum_nb[s] = ra;
+      cum_np[s] = ru;
+      ra += nb;
+      ru += PB ? (nb + PB - 1) / PB : 0;
+    }
+    if (threadIdx.x == blockDim.x - 1) {
+      int ta = 0, tu = 0;
+      for (int w = 0; w < kWarps; ++w) { ta += warp_tot[w]; tu += warp_tot[kWarps + w]; }
+      cum_nb[S] = ta;
+      cum_np[S] = tu;
+    }
+  }
+  __syncthreads();
+
+  // Sequences with nothing to attend produce zeros (their tiles never exist).
+  for (int s = blockIdx.x; s < S; s += gridDim.x) {
+    if (cum_nb[s + 1] != cum_nb[s]) continue;
+    const int n = Hkv * G * D;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) store_out<QT>(p.out, int64_t(s) * n + e, 0.f);
+  }
+
+  const int64_t T = int64_t(Hkv) * cum_nb[S];
+  const int64_t U = int64_t(Hkv) * cum_np[S];
+  const int64_t nunits = PB ? U : T;
+  const int W = int(p.num_workers < nunits ? int64_t(p.num_workers) : nunits);
+  const int w = blockIdx.x * kWarps + warp;
+  if (w >= W) return;
+
+  auto locate = [&](int64_t t) -> Tile {
+    Tile r;
+    r.s = find_seq(cum_nb, S, t, Hkv);
+    r.nb = cum_nb[r.s + 1] - cum_nb[r.s];
+    const int64_t off = t - int64_t(Hkv) * cum_nb[r.s];
+    r.h = int(off / r.nb);
+    r.b = int(off - int64_t(r.h) * r.nb);
+    r.len = clamp_len(p.context_lens[r.s], p.max_len);
+    return r;
+  };
+  // First tile of unit u (partition mode) in the flattened tile order.
+  auto unit_tile = [&](int64_t u) -> int64_t {
+    if (u >= U) return T;
+    const int s = find_seq(cum_np, S, u, Hkv);
+    const int np = cum_np[s + 1] - cum_np[s];
+    const int nb = cum_nb[s + 1] - cum_nb[s];
+    const int64_t off = u - int64_t(Hkv) * cum_np[s];
+    const int h = int(off / np), part = int(off - int64_t(h) * np);
+    return int64_t(Hkv) * cum_nb[s] + int64_t(h) * nb + int64_t(part) * PB;
+  };
+  auto start_of = [&](int64_t wi) -> int64_t { return wi * nunits / W; };
+
+  int64_t t_begin, t_end;
+  if (PB) {
+    t_begin = unit_tile(start_of(w));
+    t_end = unit_tile(start_of(w + 1));
+  } else {
+    t_begin = start_of(w);
+    t_end = start_of(w + 1);
+  }
+  const int n = int(t_end - t_begin);
+
+  uint8_t* my_stages = smem + warp * kStages * C::kStageBytes;
+  const uint64_t pol = l2_policy_evict_first();
+
+  // Walk to the next tile in flattened order (sequence, kv head, block), skipping
+  // sequences without tiles.
+  auto advance = [&](Tile& c) {
+    if (++c.b < c.nb) return;
+    c.b = 0;
+    if (++c.h < Hkv) return;
+    c.h = 0;
+    do { ++c.s; } while (c.s < S && cum_nb[c.s + 1] == cum_nb[c.s]);
+    if (c.s < S) {
+      c.nb = cum_nb[c.s + 1] - cum_nb[c.s];
+      c.len = clamp_len(p.context_lens[c.s], p.max_len);
+    }
+  };
+
+  // Lane 0 issues the TMA loads of tile c into stage st.
+  auto issue = [&](const Tile& c, int st) {
+    if (lane != 0) return;
+    const int pb = p.block_tables[int64_t(c.s) * p.max_blocks + c.b];
+    uint64_t* bar = &bars[warp][st];
+    if (pb < 0 || pb >= p.num_blocks) {
+      set_error(p.err, PKV_DEVERR_BLOCK_ID);
+      mbar_arrive(bar);                      // completes the phase without data
+      return;
+    }
+    mbar_arrive_expect_tx(bar, C::kStageBytes);
+    const int y = int((int64_t(pb) * Hkv + c.h) * kBS);
+    uint8_t* kdst = my_stages + st * C::kStageBytes;
+#pragma unroll
+    for (int bx = 0; bx < C::kNBox; ++bx) tma_load_2d(kdst + bx * 2048, &tmk, bar, bx * C::kBoxElems, y, pol);
+#pragma unroll
+    for (int bx = 0; bx < C::kNBox; ++bx)
+      tma_load_2d(kdst + C::kTileBytes + bx * 2048, &tmv, bar, bx * C::kBoxElems, y, pol);
+  };
+
+  Tile pc = locate(t_begin);                 // producer cursor, kStages tiles ahead
+  for (int i = 0; i < min(n, kStages); ++i) {
+    issue(pc, i);
+    advance(pc);
+  }
+  Tile tl = locate(t_begin);                 // consumer cursor
+
+  // Per-piece state.
+  uint32_t qf[C::kKSteps][2];
+  float o[C::kMTiles][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float sl = p.scale_log2;
+  int piece_b0 = 0;
+
+  for (int i = 0; i < n; ++i, advance(tl)) {
+    const int st = i % kStages;
+    const bool piece_start = i == 0 || tl.b == 0 || (PB && tl.b % PB == 0);
+    if (piece_start) {
+      piece_b0 = tl.b;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      sl = p.scale_log2 * (KV == KV_E4M3 ? p.k_scale[tl.h] : 1.f);
+      const bool live = gq < G;
+      const int64_t qrow = (int64_t(tl.s) * Hkv * G + int64_t(tl.h) * G + gq) * D;
+#pragma unroll
+      for (int j = 0; j < C::kKSteps; ++j) {
+        if constexpr (KV == KV_E4M3) {
+          float2 a = live ? q_pair<QT>(p.q, qrow + 32 * tq + 4 * j) : make_float2(0.f, 0.f);
+          float2 b = live ? q_pair<QT>(p.q, qrow + 32 * tq + 4 * j + 2) : make_float2(0.f, 0.f);
+          qf[j][0] = pack2<false>(a.x, a.y);
+          qf[j][1] = pack2<false>(b.x, b.y);
+        } else {
+          const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+          qf[j][0] = live ? qw[(qrow + 16 * j + 2 * tq) >> 1] : 0u;
+          qf[j][1] = live ? qw[(qrow + 16 * j + 8 + 2 * tq) >> 1] : 0u;
+        }
+      }
+    }
+
+    const int pb = p.block_tables[int64_t(tl.s) * p.max_blocks + tl.b];
+    if (!mbar_wait(&bars[warp][st], uint32_t(i / kStages) & 1u)) {
+      // Give up: report, then wait (bounded) for this warp's loads still in flight.
+      if (lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
+      for (int k = i; k < min(n, i + kStages); ++k) (void)mbar_wait(&bars[warp][k % kStages], uint32_t(k / kStages) & 1u);
+      return;
+    }
+
+    const int nv = (pb < 0 || pb >= p.num_blocks) ? 0 : min(kBS, tl.len - tl.b * kBS);
+    if (nv > 0) {
+      const uint32_t kbase = smem_u32(my_stages + st * C::kStageBytes);
+      const uint32_t vbase = kbase + C::kTileBytes;
+      // ---- S^T = K Q^T -------------------------------------------------------------
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (KV == KV_E4M3) {
+        uint32_t kr[2][8];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int row = gq + 8 * rr;
+          const uint4 c0 = lds128(kbase + swz128(row, 2 * tq));
+          const uint4 c1 = lds128(kbase + swz128(row, 2 * tq + 1));
+          kr[rr][0] = c0.x; kr[rr][1] = c0.y; kr[rr][2] = c0.z; kr[rr][3] = c0.w;
+          kr[rr][4] = c1.x; kr[rr][5] = c1.y; kr[rr][6] = c1.z; kr[rr][7] = c1.w;
+        }
+#pragma unroll
+        for (int j = 0; j < C::kKSteps; ++j) {
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(kr[0][j]);
+          a[1] = e4m3x2_to_f16x2(kr[1][j]);
+          a[2] = e4m3x2_to_f16x2(kr[0][j] >> 16);
+          a[3] = e4m3x2_to_f16x2(kr[1][j] >> 16);
+          if (j & 1) mma16816<false>(sb, a, qf[j][0], qf[j][1]);
+          else mma16816<false>(sa, a, qf[j][0], qf[j][1]);
+        }
+      } else {
+        const int mi = lane >> 3;
+        const int row = (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+        for (int j = 0; j < C::kKSteps; ++j) {
+          const int chunk = 2 * j + (mi >> 1);
+          uint32_t a[4];
+          ldsm_x4(kbase + (chunk >> 3) * 2048 + swz128(row, chunk & 7), a[0], a[1], a[2], a[3]);
+          if (j & 1) mma16816<C::kBF16>(sb, a, qf[j][0], qf[j][1]);
+          else mma16816<C::kBF16>(sa, a, qf[j][0], qf[j][1]);
+        }
+      }
+      // s[0]: (token g, head 2t)  s[1]: (token g, head 2t+1)  s[2]/s[3]: token g + 8.
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = (sa[e] + sb[e]) * sl;
+      const bool v0 = gq < nv, v8 = gq + 8 < nv;
+      if (!v0) { x[0] = -INFINITY; x[1] = -INFINITY; }
+      if (!v8) { x[2] = -INFINITY; x[3] = -INFINITY; }
+      // ---- online softmax over the tile's 16 tokens ----------------------------------
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p0 = fast_exp2(x[0] - mn0), p1 = fast_exp2(x[1] - mn1);
+      const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
+      l0 = l0 * al0 + p0 + p2;
+      l1 = l1 * al1 + p1 + p3;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+      }
+      // P^T as the B operand: lane (g, t) needs head g, tokens {2t, 2t+1} and {2t+8, 2t+9}.
+      constexpr bool kPB = C::kBF16;
+      const uint32_t pb0 = movmatrix_trans(pack2<kPB>(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack2<kPB>(p2, p3));
+      // ---- O^T += V^T P^T -----------------------------------------------------------
+      if constexpr (KV == KV_E4M3) {
+        uint4 vr[4];   // tokens 2t, 2t+1, 2t+8, 2t+9; bytes 16g .. 16g+15
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tok = 2 * tq + (k & 1) + 8 * (k >> 1);
+          vr[k] = tok < nv ? lds128(vbase + swz128(tok, gq)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const uint32_t x01[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w};
+        const uint32_t y01[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+        const uint32_t x89[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w};
+        const uint32_t y89[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+#pragma unroll
+        for (int mt = 0; mt < C::kMTiles; ++mt) {
+          const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+          const uint32_t w01 = prmt(x01[mt >> 1], y01[mt >> 1], sel);
+          const uint32_t w89 = prmt(x89[mt >> 1], y89[mt >> 1], sel);
+          uint32_t a[4];
+          a[0] = e4m3x2_to_f16x2(w01);
+          a[1] = e4m3x2_to_f16x2(w01 >> 16);
+          a[2] = e4m3x2_to_f16x2(w89);
+          a[3] = e4m3x2_to_f16x2(w89 >> 16);
+          mma16816<false>(o[mt], a, pb0, pb1);
+        }
+      } else {
+        const int mi = lane >> 3;
+        const int row = (lane & 7) + ((mi >> 1) << 3);
+        uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+        if (nv < kBS) {
+          m01 = (2 * tq < nv ? 0x0000ffffu : 0u) | (2 * tq + 1 < nv ? 0xffff0000u : 0u);
+          m89 = (2 * tq + 8 < nv ? 0x0000ffffu : 0u) | (2 * tq + 9 < nv ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::kMTiles; ++mt) {
+          const int chunk = 2 * mt + (mi & 1);
+          uint32_t a[4];
+          ldsm_x4_trans(vbase + (chunk >> 3) * 2048 + swz128(row, chunk & 7), a[0], a[1], a[2], a[3]);
+          a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
+          mma16816<C::kBF16>(o[mt], a, pb0, pb1);
+        }
+      }
+    }
+
+    // Release the stage and refill it with the tile kStages ahead.
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (i + kStages < n) {
+      issue(pc, st);
+      advance(pc);
+    }
+
+    const bool piece_end = i == n - 1 || tl.b + 1 == tl.nb || (PB && (tl.b + 1) % PB == 0);
+    if (!piece_end) continue;
+
+    // ---- finish the piece [piece_b0, tl.b] of segment (s, h) -----------------------------
+    float ls0 = l0, ls1 = l1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, off);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, off);
+    }
+    const float vs = KV == KV_E4M3 ? p.v_scale[tl.h] : 1.f;
+    const int h0 = 2 * tq, h1 = 2 * tq + 1;
+    const int Hq = Hkv * G;
+    const bool complete = piece_b0 == 0 && tl.b + 1 == tl.nb;
+    if (complete) {
+      const float inv0 = ls0 > 0.f ? vs / ls0 : 0.f, inv1 = ls1 > 0.f ? vs / ls1 : 0.f;
+      const int64_t base = (int64_t(tl.s) * Hq + int64_t(tl.h) * G) * D;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int d = out_dim<KV>(mt, r, gq);
+          if (h0 < G) store_out<QT>(p.out, base + int64_t(h0) * D + d, o[mt][2 * r] * inv0);
+          if (h1 < G) store_out<QT>(p.out, base + int64_t(h1) * D + d, o[mt][2 * r + 1] * inv1);
+        }
+      }
+      continue;
+    }
+
+    // Partial: slot, pieces of this segment, then arrive on its counter.
+    const int seg = tl.s * Hkv + tl.h;
+    const int64_t seg_t0 = int64_t(Hkv) * cum_nb[tl.s] + int64_t(tl.h) * tl.nb;
+    const int64_t seg_t1 = seg_t0 + tl.nb;
+    int npieces;
+    int64_t slot;
+    int64_t slot0 = 0;     // partition mode: first unit of the segment
+    int w0 = 0;            // balanced mode: first worker of the segment
+    bool w0_first = false;
+    if (PB) {
+      const int np = cum_np[tl.s + 1] - cum_np[tl.s];
+      slot0 = int64_t(Hkv) * cum_np[tl.s] + int64_t(tl.h) * np;
+      npieces = np;
+      slot = slot0 + piece_b0 / PB;
+    } else {
+      auto worker_of = [&](int64_t tt) {
+        int64_t wi = tt * W / nunits;
+        while (wi + 1 < W && start_of(wi + 1) <= tt) ++wi;
+        while (start_of(wi) > tt) --wi;
+        return int(wi);
+      };
+      w0 = worker_of(seg_t0);
+      const int w1 = worker_of(seg_t1 - 1);
+      npieces = w1 - w0 + 1;
+      w0_first = seg_t0 == start_of(w0);
+      slot = (w == w0 && !w0_first) ? 2 * int64_t(w) + 1 : 2 * int64_t(w);
+    }
+    {
+      float* po = p.po + slot * G * D;
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int d = out_dim<KV>(mt, r, gq);
+          if (h0 < G) po[h0 * D + d] = o[mt][2 * r] * vs;
+          if (h1 < G) po[h1 * D + d] = o[mt][2 * r + 1] * vs;
+        }
+      }
+      if (gq == 0) {
+        if (h0 < G) p.ml[slot * G + h0] = make_float2(m0, ls0);
+        if (h1 < G) p.ml[slot * G + h1] = make_float2(m1, ls1);
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) old = atomicAdd(p.counters + seg, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != npieces - 1) continue;
+
+    // Last piece to arrive: merge every piece of the segment by log-sum-exp.
+    __threadfence();
+    constexpr int kVec = D / 32;   // head_dim elements per lane
+    for (int hh = 0; hh < G; ++hh) {
+      auto slot_of = [&](int k) -> int64_t {
+        if (PB) return slot0 + k;
+        return (k == 0 && !w0_first) ? 2 * int64_t(w0) + 1 : 2 * int64_t(w0 + k);
+      };
+      float M = -INFINITY;
+      for (int k = lane; k < npieces; k += 32) M = fmaxf(M, __ldcg(&p.ml[slot_of(k) * G + hh]).x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float acc[kVec];
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
+      float den = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll 4
+        for (int k = 0; k < npieces; ++k) {
+          const int64_t sk = slot_of(k);
+          const float2 ml = __ldcg(&p.ml[sk * G + hh]);
+          const float wk = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+          den += wk * ml.y;
+          const float* src = p.po + (sk * G + hh) * D + lane * kVec;
+          if constexpr (kVec == 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+            acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
+          } else {
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+            acc[0] += wk * v.x; acc[1] += wk * v.y;
+          }
+        }
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const int64_t obase = (int64_t(tl.s) * Hq + int64_t(tl.h) * G + hh) * D + lane * kVec;
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) store_out<QT>(p.out, obase + e, acc[e] * inv);
+    }
+    if (lane == 0) p.counters[seg] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------
+struct Layout {
+  size_t counters = 0, ml = 0, po = 0, total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int64_t num_slots(int num_seqs, int num_kv_heads, int max_context_len, int part_blocks, int workers) {
+  if (part_blocks == 0) return 2 * int64_t(workers);
+  const int64_t nb = (int64_t(std::max(max_context_len, 0)) + kBS - 1) / kBS;
+  return int64_t(num_seqs) * num_kv_heads * ((nb + part_blocks - 1) / part_blocks);
+}
+
+Layout layout(int num_seqs, int num_kv_heads, int group, int head_dim, int64_t slots) {
+  Layout l;
+  l.counters = 0;
+  l.ml = align256(sizeof(int) * size_t(num_seqs) * num_kv_heads);
+  l.po = l.ml + align256(sizeof(float2) * size_t(slots) * group);
+  l.total = l.po + align256(sizeof(float) * size_t(slots) * group * head_dim);
+  return l;
+}
+
+template <int KV, int D>
+size_t smem_bytes(int num_seqs) {
+  return 1024 + size_t(kWarps) * kStages * Cfg<KV, D>::kStageBytes + 2 * sizeof(int) * size_t(num_seqs + 1);
+}
+
+template <int KV, int QT, int D>
+pkv_status launch(const DecodeParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                  cudaStream_t stream) {
+  auto kern = paged_decode_kernel<KV, QT, D>;
+  const size_t smem = smem_bytes<KV, D>(prm.num_seqs);
+  if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  kern<<<grid, kWarps * 32, smem, stream>>>(tk, tv, prm);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int decode_grid() { return std::max(1, num_sms()); }
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int max_context_len, int partition_size) {
+  using namespace pkv;
+  if (num_seqs <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || block_size != kBS || partition_size < 0 ||
+      partition_size % kBS)
+    return 0;
+  const int group = num_heads / num_kv_heads;
+  const int workers = decode_grid() * kWarps;
+  const int64_t slots = num_slots(num_seqs, num_kv_heads, max_context_len, partition_size / kBS, workers);
+  return layout(num_seqs, num_kv_heads, group, head_dim, slots).total;
+}
+
+pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                            const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int max_context_len, float scale, int partition_size, void* workspace,
+                            size_t workspace_bytes, pkv_stream_t stream) {
+  using namespace pkv;
+  pkv_status st = check_cache_desc(cache);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || partition_size < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads % cache->num_kv_heads) return PKV_ERR_INVALID_ARG;
+  if (partition_size % kBS) return PKV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
+  const int group = num_heads / cache->num_kv_heads;
+  if (cache->block_size != kBS || group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  const int D = cache->head_dim;
+  if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != PKV_FP8_E4M3 && cache->kv_dtype != q_dtype) return PKV_ERR_UNSUPPORTED;
+  if (cache->kv_dtype == PKV_FP8_E4M3 && D != 128) return PKV_ERR_UNSUPPORTED;
+  if (int64_t(cache->num_blocks) * cache->num_kv_heads * kBS >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+
+  const int grid = decode_grid();
+  const int part_blocks = partition_size / kBS;
+  const int64_t slots = num_slots(num_seqs, cache->num_kv_heads, max_context_len, part_blocks, grid * kWarps);
+  const Layout lay = layout(num_seqs, cache->num_kv_heads, group, D, slots);
+  if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  unsigned* err = error_word_ptr();
+  if (!err) return PKV_ERR_CUDA;
+
+  // Tensor maps: the pool as rows of head_dim elements, boxes of 16 rows x 128 bytes.
+  CUtensorMap tk, tv;
+  const bool fp8 = cache->kv_dtype == PKV_FP8_E4M3;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * kBS;
+  const uint64_t row_bytes = uint64_t(D) * dtype_bytes(cache->kv_dtype);
+  const uint32_t box0 = fp8 ? 128 : 64;
+  if (!encode_tmap_2d(&tk, dt, k_cache, D, rows, row_bytes, box0, kBS, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tv, dt, v_cache, D, rows, row_bytes, box0, kBS, CU_TENSOR_MAP_SWIZZLE_128B))
+    return PKV_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams prm;
+  prm.out = out;
+  prm.q = q;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.k_scale = cache->k_scale;
+  prm.v_scale = cache->v_scale;
+  prm.num_seqs = num_seqs;
+  prm.num_kv_heads = cache->num_kv_heads;
+  prm.group = group;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.max_len = int(std::min<int64_t>(int64_t(max_blocks_per_seq) * kBS, max_context_len));
+  prm.num_blocks = cache->num_blocks;
+  prm.part_blocks = part_blocks;
+  prm.num_workers = grid * kWarps;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.counters = reinterpret_cast<int*>(ws + lay.counters);
+  prm.ml = reinterpret_cast<float2*>(ws + lay.ml);
+  prm.po = reinterpret_cast<float*>(ws + lay.po);
+  prm.err = err;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool qbf = q_dtype == PKV_BF16;
+  switch (cache->kv_dtype) {
+    case PKV_BF16:
+      return D == 128 ? launch<KV_BF16, KV_BF16, 128>(prm, tk, tv, grid, s)
+                      : launch<KV_BF16, KV_BF16, 64>(prm, tk, tv, grid, s);
+    case PKV_F16:
+      return D == 128 ? launch<KV_F16, KV_F16, 128>(prm, tk, tv, grid, s)
+                      : launch<KV_F16, KV_F16, 64>(prm, tk, tv, grid, s);
+    case PKV_FP8_E4M3:
+      return qbf ? launch<KV_E4M3, KV_BF16, 128>(prm, tk, tv, grid, s)
+                 : launch<KV_E4M3, KV_F16, 128>(prm, tk, tv, grid, s);
+  }
+  return PKV_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

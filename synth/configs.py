@@ -130,7 +130,7 @@ def make_decode_case(name: str, seed: int, lens: List[int], num_heads: int, num_
     unique_before = sum(n_before) - shared_dups + chunk_blocks_before
     needed_after = n_after_total - shared_dups + chunk_blocks_after + copy_pairs
     if num_blocks is None:
-        num_blocks = int(math.ceil(pool_slack * needed_after))
+        num_blocks = max(1, int(math.ceil(pool_slack * needed_after)))
     assert num_blocks >= needed_after, "pool too small for the step"
     perm = torch.randperm(num_blocks, generator=g).tolist()
     nxt = 0

@@ -1,0 +1,203 @@
+"""CPU tests of the C ABI library: every declared symbol is exported, argument checks
+refuse bad inputs without a GPU, and the C++ block manager matches the oracle's block
+manager model bit for bit (and the pages' printed capacity numbers)."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    return sorted(set(re.findall(r"PKV_API[^;(]*?\b(pkv_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    import paged_kv_cache_160_gb300 as pkv
+    names = _declared_symbols()
+    assert len(names) >= 20
+    raw = ctypes.CDLL(pkv._binding._LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in include/pkv.h but not exported"
+
+
+def test_status_strings_and_version():
+    import paged_kv_cache_160_gb300 as pkv
+    assert pkv.lib.pkv_status_string(0) == b"ok"
+    assert pkv.lib.pkv_status_string(5) == b"no free blocks"
+    assert pkv.lib.pkv_version() >= 1
+
+
+def test_argument_checks_run_on_host_without_gpu():
+    import paged_kv_cache_160_gb300 as pkv
+    from paged_kv_cache_160_gb300._binding import CacheDesc
+    L = pkv.lib
+    desc = CacheDesc(64, 4, 16, 128, 1, None, None)
+    # bad GQA split
+    assert L.pkv_paged_decode(16, 16, 1, 4, 6, 16, 16, ctypes.byref(desc), 16, 8, 16, 128, 0.1, 0, 16, 1 << 20,
+                              None) == 1
+    # partition not a multiple of the block size
+    assert L.pkv_paged_decode(16, 16, 1, 4, 8, 16, 16, ctypes.byref(desc), 16, 8, 16, 128, 0.1, 24, 16, 1 << 20,
+                              None) == 1
+    # unsupported head_dim
+    d96 = CacheDesc(64, 4, 16, 96, 1, None, None)
+    assert L.pkv_paged_decode(16, 16, 1, 4, 8, 16, 16, ctypes.byref(d96), 16, 8, 16, 128, 0.1, 0, 16, 1 << 20,
+                              None) == 2
+    # misaligned pointer
+    assert L.pkv_kv_write(17, 16, 1, 4, 16, 16, 16, ctypes.byref(desc), None) == 1
+    # e4m3 cache without scales
+    d8 = CacheDesc(64, 4, 16, 128, 2, None, None)
+    assert L.pkv_copy_blocks(16, 16, ctypes.byref(d8), 16, 1, None) == 1
+    # nothing to do is fine
+    assert L.pkv_kv_write(16, 16, 1, 0, 16, 16, 16, ctypes.byref(desc), None) == 0
+    assert L.pkv_copy_blocks(16, 16, ctypes.byref(desc), 16, 0, None) == 0
+    assert L.pkv_decode_workspace_bytes(4, 6, 4, 128, 16, 100, 0) == 0       # bad split -> 0
+
+
+# ---------------------------------------------------------------------------------------
+# block manager: pins and parity with the oracle model
+# ---------------------------------------------------------------------------------------
+
+def test_capacity_model_printed_output(golden_dir):
+    from paged_kv_cache_160_gb300 import BlockManager, NoBlocksError
+    fx = json.load(open(os.path.join(golden_dir, "capacity_model.json")))
+    bm = BlockManager(fx["pool_blocks"], fx["block_size"])
+    n = 0
+    for i, L in enumerate(fx["lens"]):
+        try:
+            bm.allocate(i, L)
+        except NoBlocksError:
+            break
+        n += 1
+    assert n == fx["expected"]["paged_admitted"]
+    assert fx["pool_blocks"] - bm.num_free() == fx["expected"]["paged_used_blocks"]
+
+
+def test_lecture33_figure_and_cow(golden_dir):
+    from paged_kv_cache_160_gb300 import BlockManager
+    fx = json.load(open(os.path.join(golden_dir, "block_table_diagrams.json")))["lecture33_figure"]
+    bm = BlockManager(fx["num_blocks"], fx["block_size"])
+    bm.import_seq(0, [7, 2, 5], 10)
+    bm.import_seq(1, [7, 9], 6)
+    for b, r in fx["ref_cnt"].items():
+        assert bm.ref_cnt(int(b)) == r
+    # fork B, then the child writes into the shared, half-full block 9 -> copy-on-write
+    bm.fork(1, 2)
+    assert bm.ref_cnt(9) == 2 and bm.ref_cnt(7) == 3
+    slot, cow = bm.append_slot(2)
+    assert cow is not None and cow[0] == 9
+    assert bm.ref_cnt(9) == 1 and bm.ref_cnt(cow[1]) == 1
+    assert slot == cow[1] * 4 + 2
+
+
+def test_step_decode_is_all_or_nothing():
+    from paged_kv_cache_160_gb300 import BlockManager, NoBlocksError
+    bm = BlockManager(3, 16)
+    bm.allocate(0, 16)
+    bm.allocate(1, 16)
+    before = bm.free_queue()
+    with pytest.raises(NoBlocksError):          # both sequences need a new block, only one is free
+        bm.step_decode([0, 1], 4)
+    assert bm.free_queue() == before and bm.export([0, 1], 4)[1] == [16, 16]
+
+
+def _random_ops(seed, n_ops=3000, nb=300, bs=16):
+    rng = np.random.default_rng(seed)
+    ops = []
+    live, nxt = [], 0
+    for _ in range(n_ops):
+        r = rng.random()
+        if r < 0.2 or not live:
+            ops.append(("allocate", nxt, int(rng.integers(0, 120)))); live.append(nxt); nxt += 1
+        elif r < 0.55:
+            ops.append(("append_slot", int(rng.choice(live))))
+        elif r < 0.65:
+            ops.append(("append_slots", int(rng.choice(live)), int(rng.integers(1, 40))))
+        elif r < 0.75:
+            ops.append(("fork", int(rng.choice(live)), nxt)); live.append(nxt); nxt += 1
+        elif r < 0.85:
+            k = int(rng.integers(1, min(8, len(live)) + 1))
+            ops.append(("step_decode", [int(x) for x in rng.choice(live, size=k, replace=False)]))
+        else:
+            s = int(rng.choice(live)); ops.append(("free", s)); live.remove(s)
+    return ops
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_block_manager_matches_oracle_model(seed):
+    from oracle.block_manager import BlockManagerModel, NoBlocks
+    from paged_kv_cache_160_gb300 import BlockManager, NoBlocksError
+    nb, bs, mb = 300, 16, 64
+    model, prod = BlockManagerModel(nb, bs), BlockManager(nb, bs)
+    live = set()
+    for op in _random_ops(seed, nb=nb, bs=bs):
+        kind = op[0]
+        if kind == "step_decode":
+            seqs = [s for s in op[1] if s in live]
+            if not seqs:
+                continue
+            # the model has no batch call: all-or-nothing on the number of blocks needed
+            try:
+                got = prod.step_decode(seqs, mb)
+            except NoBlocksError:
+                got = None
+            if got is None:
+                continue
+            slots, cows = [], []
+            for s in seqs:
+                sl, c = model.append_slot(s)
+                slots.append(sl)
+                if c is not None:
+                    cows.append(c)
+            tables, lens = model.export(seqs, mb)
+            assert got == (slots, cows, tables, lens)
+            continue
+        if kind in ("append_slot", "append_slots", "free", "fork") and op[1] not in live:
+            continue
+        res = {}
+        for name, side in (("m", model), ("p", prod)):
+            try:
+                if kind == "allocate":
+                    side.allocate(op[1], op[2]); res[name] = "ok"
+                elif kind == "append_slot":
+                    res[name] = side.append_slot(op[1])
+                elif kind == "append_slots":
+                    res[name] = side.append_slots(op[1], op[2])
+                elif kind == "fork":
+                    side.fork(op[1], op[2]); res[name] = "ok"
+                elif kind == "free":
+                    side.free(op[1]); res[name] = "ok"
+            except (NoBlocks, NoBlocksError):
+                res[name] = "noblocks"
+        assert res["m"] == res["p"], op
+        if res["p"] == "ok":
+            if kind == "allocate":
+                live.add(op[1])
+            elif kind == "fork":
+                live.add(op[2])
+            elif kind == "free":
+                live.discard(op[1])
+        assert prod.num_free() == model.num_free()
+    assert prod.free_queue() == list(model.free_queue)
+    assert [prod.ref_cnt(b) for b in range(nb)] == model.ref_cnt
+    seqs = sorted(live)
+    assert prod.export(seqs, mb) == model.export(seqs, mb)
+
+
+def test_synthetic_plans_agree_on_both_sides():
+    """The tiny workload's step: copy-on-write for sequence 0, a new block for sequence 3."""
+    import synth
+    from tests.harness import oracle_plan, product_plan
+    case = synth.tiny_config()
+    po, pp = oracle_plan(case), product_plan(case)
+    assert po == pp
+    assert len(pp.cows) == 1 and pp.cows[0][0] == case.seq_blocks[0][0]
+    assert pp.lens == [11, 7, 38, 17]
+    assert pp.tables[3][0] == case.seq_blocks[3][0] != pp.tables[0][0]
+    # sequence 2's new token is token 37: logical block 2, offset 5 (the worked example)
+    assert pp.slots[2] == case.seq_blocks[2][2] * 16 + 5
