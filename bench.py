@@ -1,0 +1,429 @@
+"""Benchmark of the paged-KV decode step on GB300: effective HBM GB/s and seq-tokens/s.
+
+Workload: the Qwen2.5-7B-shaped GQA decode batch — 64 running sequences with context
+lengths uniform in [128, 2048], 28 query heads / 4 kv heads, head_dim 128, bf16 Q/K/V,
+16-token blocks in a shuffled pool ([num_blocks, 4, 16, 128], pool = blocks needed + 10%).
+One step = plan the step on the host block manager (done once; its cost is reported
+separately), kv_write of the 64 new tokens, then paged_decode over every sequence's
+L + 1 tokens (one launch: split-KV and merge).
+
+Timing: CUDA events on the launching stream.  The kernels of a step are captured once
+per pool copy into CUDA graphs; the timed loop replays them.  Every step uses the next of
+R pool copies whose combined size is above 3x the L2 size, so no step finds its K/V in L2.
+`value` is device-resident throughput; `e2e` adds, every step, the pinned host->device
+copies of the step's inputs (q, new K/V, slots, tables, lengths) and the device->host copy
+of the output.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU baseline times the oracle with one BLAS thread; pin numpy's BLAS before it loads.
+for _var in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+    os.environ.setdefault(_var, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode effective HBM GB/s (% of GB300 peak); seq-tokens attended/s"
+WORKLOAD = ("qwen2.5-7b-gqa paged decode step: 64 seqs, context_lens U[128,2048] (seed 1602), "
+            "28 q heads / 4 kv heads, head_dim 128, bf16, block_size 16, kv_write 64 tokens + paged_decode")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per paged_decode launch on this workload from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel source with
+# this hash; when the source changes, traffic is reported as null until re-measured.
+TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+
+
+def _src_hash() -> str:
+    h = hashlib.sha1()
+    for f in ("paged_decode.cu", "pkv_device.cuh"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_160_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def workload_bytes(case, plan):
+    """Algorithmic bytes of one step (each unique attended K/V row once)."""
+    Hkv, D, Hq = case.num_kv_heads, case.head_dim, case.num_heads
+    kv_elt = 1 if case.kv_dtype == "e4m3" else 2
+    q_elt = 2
+    unique_rows = set()
+    for t, L in zip(plan.tables, plan.lens):
+        for j in range(L):
+            unique_rows.add(t[j // 16] * 16 + j % 16)
+    n_rows = len(unique_rows)
+    nblocks = sum(-(-L // 16) for L in plan.lens)
+    S = case.num_seqs
+    decode = 2 * n_rows * Hkv * D * kv_elt + 2 * S * Hq * D * q_elt + 4 * nblocks + 4 * S
+    T = len(plan.slots)
+    write = 2 * 2 * T * Hkv * D * kv_elt + 8 * T
+    return decode, write, sum(plan.lens)
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_160_gb300 as pkv
+    import synth
+    from tests.harness import product_plan
+
+    ws_n, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    case = synth.qwen7b_gqa_config()
+    t0 = time.perf_counter()
+    plan = product_plan(case)
+    host_plan_us = (time.perf_counter() - t0) * 1e6
+    decode_bytes, write_bytes, tokens = workload_bytes(case, plan)
+    step_bytes = decode_bytes + write_bytes
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024
+    pool_bytes = 2 * case.k_cache.numel() * case.k_cache.element_size()
+    R = max(2, math.ceil(3 * l2 / pool_bytes) + 1)
+    kcs = [case.k_cache.to(dev) for _ in range(R)]
+    vcs = [case.v_cache.to(dev) for _ in range(R)]
+    desc = pkv.cache_desc(kcs[0])
+    descs = [pkv.cache_desc(k) for k in kcs]
+    q = case.q.to(dev)
+    k_new = case.k_new.to(dev)
+    v_new = case.v_new.to(dev)
+    slots = torch.tensor(plan.slots, dtype=torch.int64, device=dev)
+    tables = torch.tensor(plan.tables, dtype=torch.int32, device=dev)
+    lens = torch.tensor(plan.lens, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    max_len = max(plan.lens)
+    part = 0
+    wsb = pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim, 16,
+                                         max_len, part)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def write(r):
+        pkv.pkv_kv_write(k_new, v_new, slots, kcs[r], vcs[r], descs[r])
+
+    def decode(r):
+        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, part, ws)
+
+    # eager warm-up (also initialises the library's per-device state before capture)
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            write(r)
+            decode(r)
+    stream.synchronize()
+    assert pkv.pkv_get_device_error(stream) == 0
+    g_write, g_dec = [], []
+    for r in range(R):
+        gw, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw, stream=stream, capture_error_mode="thread_local"):
+            write(r)
+        with torch.cuda.graph(gd, stream=stream, capture_error_mode="thread_local"):
+            decode(r)
+        g_write.append(gw)
+        g_dec.append(gd)
+    torch.cuda.synchronize(dev)
+
+    K, W = args.steps, args.warmup
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if ws_n > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for k in range(W):
+            g_write[k % R].replay()
+            g_dec[k % R].replay()
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for k in range(K):
+                r = (W + k) % R
+                g_write[r].replay()
+                ev_a[k].record(stream)
+                g_dec[r].replay()
+                ev_b[k].record(stream)
+            end.record(stream)
+        stream.synchronize()
+    barrier()
+    torch.cuda.synchronize(dev)
+    elapsed_ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    if ws_n > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    assert pkv.pkv_get_device_error(stream) == 0
+
+    # ---- end to end: host buffers, copies inside the timed region -----------------------
+    h_q = case.q.pin_memory()
+    h_kn = case.k_new.pin_memory()
+    h_vn = case.v_new.pin_memory()
+    h_slots = torch.tensor(plan.slots, dtype=torch.int64).pin_memory()
+    h_tables = torch.tensor(plan.tables, dtype=torch.int32).pin_memory()
+    h_lens = torch.tensor(plan.lens, dtype=torch.int32).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_tables, h_lens))
+    d2h = h_out.numel() * h_out.element_size()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for k in range(K):
+            r = (W + k) % R
+            q.copy_(h_q, non_blocking=True)
+            k_new.copy_(h_kn, non_blocking=True)
+            v_new.copy_(h_vn, non_blocking=True)
+            slots.copy_(h_slots, non_blocking=True)
+            tables.copy_(h_tables, non_blocking=True)
+            lens.copy_(h_lens, non_blocking=True)
+            g_write[r].replay()
+            g_dec[r].replay()
+            h_out.copy_(out, non_blocking=True)
+        e_end.record(stream)
+    stream.synchronize()
+    barrier()
+    e2e_ms = e_start.elapsed_time(e_end)
+    if ws_n > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert torch.equal(h_out.to(dev), out)
+
+    peak, peak_kind = _peaks()
+    ms_per_step = elapsed_ms / K
+    value = ws_n * step_bytes / (ms_per_step * 1e-3) / 1e9
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha1"] == _src_hash() else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws_n,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, shuffled physical block ids)",
+        "config": {"workload": WORKLOAD, "num_seqs": case.num_seqs, "attended_tokens": tokens,
+                   "step_bytes": step_bytes, "decode_bytes": decode_bytes, "kv_write_bytes": write_bytes,
+                   "pool_copies": R, "l2": f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB > 3x L2)",
+                   "launch": "CUDA graph replay per kernel", "partition_size": part,
+                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
+        "seq_tokens_per_s": round(ws_n * tokens / (ms_per_step * 1e-3), 1),
+        "pct_of_nominal_8tbs": round(100 * value / ws_n / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_copy": round(100 * value / ws_n / peak, 2),
+        "roofline": {"kernel": "paged_decode", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "e2e": {"value": round(ws_n * step_bytes / (e2e_ms / K * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "host_plan_us": round(host_plan_us, 1),
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(case, plan, decode_bytes, write_bytes)
+        print(json.dumps(line))
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _oracle_step(case, plan, seqs):
+    """The oracle (as it stands) on a subset of the step: its KV write and decode."""
+    import numpy as np
+    from oracle import cache_ops, paged_attention as pa
+    from tests.harness import codes, q_f64
+    k, v = codes(case.k_cache), codes(case.v_cache)
+    k, v = cache_ops.kv_write(k, v, codes(case.k_new)[seqs], codes(case.v_new)[seqs], [plan.slots[i] for i in seqs])
+    q = q_f64(case.q)[seqs]
+    pa.decode_attention(q, k, v, case.kv_dtype, [plan.tables[i] for i in seqs], [plan.lens[i] for i in seqs],
+                        case.scale)
+
+
+def _sample_bytes(case, plan, seqs):
+    Hkv, D = case.num_kv_heads, case.head_dim
+    rows = sum(plan.lens[i] for i in seqs)
+    return (2 * rows * Hkv * D * 2 + 2 * len(seqs) * case.num_heads * D * 2 + 4 * len(seqs)
+            + 2 * 2 * len(seqs) * Hkv * D * 2 + 8 * len(seqs)), rows
+
+
+def cpu_baseline(case, plan, decode_bytes, write_bytes, budget_s: float = 12.0):
+    """Times the fp64 oracle on the host cores, single-threaded BLAS, cycling over the batch."""
+    seqs_all = list(range(case.num_seqs))
+    done_bytes = done_tokens = 0
+    n_seq = 0
+    t0 = time.perf_counter()
+    if True:
+        i = 0
+        while time.perf_counter() - t0 < budget_s and n_seq < 4 * case.num_seqs:
+            seqs = [seqs_all[(i + j) % case.num_seqs] for j in range(8)]
+            _oracle_step(case, plan, seqs)
+            b, rows = _sample_bytes(case, plan, seqs)
+            done_bytes += b
+            done_tokens += rows
+            n_seq += len(seqs)
+            i += 8
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seq_tokens_per_s": round(done_tokens / dt, 1),
+            "sample": f"fp64 numpy oracle (kv_write + decode) on {n_seq} sequence-steps of the same workload, "
+                      f"8 sequences per call, {dt:.1f} s wall, 1 BLAS thread"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample (4 sequences)."""
+    import synth
+    from tests.harness import oracle_plan
+    ws_n, rank, _ = _dist()
+    if rank != 0:
+        return
+    case = synth.qwen7b_gqa_config()
+    plan = oracle_plan(case)
+    per = 4
+    if True:
+        for k in range(args.warmup):
+            _oracle_step(case, plan, [(k * per + j) % case.num_seqs for j in range(per)])
+        tot_b = tot_rows = 0
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            seqs = [((args.warmup + k) * per + j) % case.num_seqs for j in range(per)]
+            _oracle_step(case, plan, seqs)
+            b, rows = _sample_bytes(case, plan, seqs)
+            tot_b += b
+            tot_rows += rows
+        dt = time.perf_counter() - t0
+    value = tot_b / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws_n,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample_per_step": f"{per} sequences"},
+            "seq_tokens_per_s": round(tot_rows / dt, 1),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{per} sequences of the workload per step (kv_write + decode), fp64 numpy, "
+                                       "1 BLAS thread"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

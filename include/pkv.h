@@ -116,11 +116,11 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache
                            const int32_t* block_pairs, int num_pairs, pkv_stream_t stream);
 
 /*
- * Workspace bytes pkv_paged_decode needs on the current device (split-KV partials and
- * per-(sequence, kv head) merge counters).  partition_size = 0 selects the balanced
- * split (work cut evenly over all SMs); > 0 cuts every sequence into partitions of that
- * many tokens (a multiple of block_size).  Zero the workspace once after allocating it;
- * every decode call leaves its counters at zero again.
+ * Workspace bytes pkv_paged_decode needs on the current device: two partial-result
+ * slots per worker warp (running max, sum of exponentials and unnormalised output per
+ * query head) plus one piece descriptor per (sequence, kv head).  It depends on the
+ * device's SM count, not on the context lengths.  The workspace needs no initialisation;
+ * each call rewrites what it reads.  Calls that share a workspace must not overlap.
  */
 PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                   int block_size, int max_context_len, int partition_size);
@@ -130,16 +130,21 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_k
  * i, query head h and kv head g = h / (num_heads / num_kv_heads), with L = context_lens[i]:
  *   s_j = scale * q[i][h] . K_i[j]  for j < L, where K_i[j] = k_cache[T_i[j / B]][g][j % B]
  *   out[i][h] = sum_j softmax(s)_j V_i[j]                         (zeros when L == 0)
- * with T_i = block_tables[i].  Computed as an online softmax per KV split followed by a
- * log-sum-exp merge of the splits, fp32 accumulation.
+ * with T_i = block_tables[i].  Split-KV: the (sequence, kv head, block) tiles are cut into
+ * one contiguous range per worker warp — at any block (partition_size = 0, "balanced")
+ * or only at multiples of partition_size tokens.  A worker runs an online softmax over
+ * its range (consecutive partitions merge in registers); pieces of one sequence held by
+ * different workers are merged by log-sum-exp in a second kernel on the same stream,
+ * launched as a programmatic dependent of the first.  fp32 accumulation.
  *   out            (device) [num_seqs][num_heads][head_dim] of q_dtype
  *   q              (device) [num_seqs][num_heads][head_dim] of q_dtype (f16 or bf16)
  *   block_tables   (device) int32 [num_seqs][max_blocks_per_seq]
  *   context_lens   (device) int32 [num_seqs]; tokens to attend, including any token
  *                  written this step
- *   max_context_len host upper bound of context_lens (sizes the partitioned workspace)
- *   partition_size  0 = balanced split; else tokens per partition (multiple of block_size)
- *   workspace       (device) >= pkv_decode_workspace_bytes(...) bytes, zeroed once
+ *   max_context_len host upper bound of context_lens; larger lengths are clamped to it
+ *                  (and to max_blocks_per_seq * block_size) and flagged PKV_DEVERR_CONTEXT_LEN
+ *   partition_size  0 = balanced split; else split granularity in tokens (multiple of block_size)
+ *   workspace       (device) >= pkv_decode_workspace_bytes(...) bytes
  * Supported: kv f16/bf16 with the same q dtype, or e4m3 kv with f16/bf16 q (the e4m3
  * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16;
  * num_heads / num_kv_heads in 1..8.

@@ -139,10 +139,16 @@ def _stream(stream) -> int:
 
 def cache_desc(k_cache: torch.Tensor, k_scale: Optional[torch.Tensor] = None,
                v_scale: Optional[torch.Tensor] = None) -> CacheDesc:
-    """Descriptor of a pool tensor shaped [num_blocks, num_kv_heads, block_size, head_dim]."""
+    """Descriptor of a pool tensor shaped [num_blocks, num_kv_heads, block_size, head_dim].
+
+    The descriptor holds raw pointers to the scale tensors, so it keeps references to
+    them: the memory stays valid for as long as the descriptor lives.
+    """
     nb, hkv, bs, d = k_cache.shape
-    return CacheDesc(nb, hkv, bs, d, pkv_dtype_of(k_cache), _dev(k_scale, "k_scale") or None,
+    desc = CacheDesc(nb, hkv, bs, d, pkv_dtype_of(k_cache), _dev(k_scale, "k_scale") or None,
                      _dev(v_scale, "v_scale") or None)
+    desc._keep = (k_scale, v_scale)
+    return desc
 
 
 def pkv_kv_write(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kThreads) kv_write_copy_kernel(const uint4* __
                                                                  uint4* __restrict__ v_cache, int num_tokens,
                                                                  int num_kv_heads, int chunks, int block_size,
                                                                  int64_t num_slots, unsigned* err) {
+  griddep_launch_dependents();   // a following decode may start its length-only prologue
   const int64_t total = int64_t(num_tokens) * num_kv_heads * chunks;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     const int c = int(i % chunks);
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(kThreads) kv_write_quant_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const float* __restrict__ k_scale,
     const float* __restrict__ v_scale, int num_tokens, int num_kv_heads, int chunks, int block_size,
     int64_t num_slots, unsigned* err) {
+  griddep_launch_dependents();
   const int64_t total = int64_t(num_tokens) * num_kv_heads * chunks;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     const int c = int(i % chunks);

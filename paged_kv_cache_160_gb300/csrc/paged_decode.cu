@@ -11,9 +11,10 @@
 // GB300 design
 //   * Work unit = one (sequence, kv head, logical block) tile: 16 tokens x head_dim of K and
 //     of V, each a contiguous run in the [block][kv_head][row][dim] pool.
-//   * Persistent grid, one CTA per SM, 4 independent worker warps per CTA.  The flattened
+//   * Persistent grid, one CTA per SM, 12 independent worker warps per CTA.  The flattened
 //     tile list (sequence-major, kv head, block) is cut into equal contiguous ranges, one
-//     per worker ("balanced" split), or into fixed partitions of partition_size tokens.
+//     per worker ("balanced" split), or into equal runs of whole partition_size-token
+//     partitions.  A worker's online softmax runs across consecutive partitions.
 //   * Each worker warp owns a ring of TMA stages: lane 0 issues 2-D tensor loads of the K
 //     and V tile (128-byte swizzled) straight from the physical block named by the block
 //     table, completing on an mbarrier; the warp waits, computes, and refills the stage.
@@ -24,9 +25,11 @@
 //     the fragments are loaded with plain shared loads in a head_dim/token order chosen so
 //     every lane reads 16 contiguous bytes, and converted exactly to fp16.
 //   * A range that covers only part of a (sequence, kv head) writes a partial (m, l, o) to
-//     the workspace; the last arriving piece (atomic counter, no waiting) merges all pieces
-//     by log-sum-exp and resets the counter, so one launch does split + merge.
+//     the workspace (at most two per worker); the last arriving piece (atomic counter, no
+//     waiting) merges all pieces by log-sum-exp and resets the counter, so one launch does
+//     split + merge.
 #include <algorithm>
+#include <utility>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -37,8 +40,7 @@ namespace {
 enum { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
 
 constexpr int kBS = 16;        // tokens per block
-constexpr int kWarps = 4;      // worker warps per CTA
-constexpr int kStages = 4;     // TMA stages per worker warp
+constexpr int kMaxWarps = 12;  // worker warps per CTA (3 per SM sub-partition)
 constexpr int kMaxGroup = 8;   // query heads per kv head handled by one n=8 MMA tile
 
 template <int KV, int D>
@@ -70,9 +72,9 @@ struct DecodeParams {
   int max_len;            // min(max_blocks * 16, max_context_len): lengths are clamped to it
   int num_blocks;
   int part_blocks;        // blocks per partition; 0 = balanced split
-  int num_workers;        // gridDim.x * kWarps
+  int num_workers;        // gridDim.x * worker warps per CTA
   float scale_log2;       // softmax scale * log2(e)
-  int* counters;          // [num_seqs * num_kv_heads]
+  int4* seg_desc;         // [num_seqs * num_kv_heads]: (first worker, pieces, first worker's slot parity, 0)
   float2* ml;             // [slots][group] (running max in log2 units, sum of exponentials)
   float* po;              // [slots][group][D] unnormalised partial outputs
   unsigned* err;
@@ -119,7 +121,7 @@ __device__ __forceinline__ int out_dim(int i, int r, int g) {
   else return 16 * i + g + 8 * r;
 }
 
-template <int KV, int QT, int D>
+template <int KV, int QT, int D, int kWarps, int kStages>
 __global__ void __launch_bounds__(kWarps * 32, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeParams p) {
@@ -187,12 +189,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
   }
   __syncthreads();
+  // Everything above reads only lengths; from here on the kernel reads the cache and
+  // writes outputs, so it waits for the preceding kernel (a KV write) to finish.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // Sequences with nothing to attend produce zeros (their tiles never exist).
   for (int s = blockIdx.x; s < S; s += gridDim.x) {
     if (cum_nb[s + 1] != cum_nb[s]) continue;
     const int n = Hkv * G * D;
     for (int e = threadIdx.x; e < n; e += blockDim.x) store_out<QT>(p.out, int64_t(s) * n + e, 0.f);
+    if (threadIdx.x < Hkv) p.seg_desc[s * Hkv + threadIdx.x] = make_int4(0, 0, 0, 0);
   }
 
   const int64_t T = int64_t(Hkv) * cum_nb[S];
@@ -251,16 +258,36 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
   };
 
-  // Lane 0 issues the TMA loads of tile c into stage st.
-  auto issue = [&](const Tile& c, int st) {
+  // Block ids of the worker's tiles, 32 per window: lane l holds the id of tile
+  // 32 * window + l of the range.  The next window is loaded one window ahead so the
+  // table lookups never sit on the path from one TMA issue to the next.
+  auto load_window = [&](int win) -> int {
+    const int64_t t = t_begin + int64_t(win) * 32 + lane;
+    if (t >= t_end) return -1;
+    const Tile c = locate(t);
+    return p.block_tables[int64_t(c.s) * p.max_blocks + c.b];
+  };
+  int bid_cur = load_window(0);
+  int bid_nxt = n > 32 ? load_window(1) : -1;
+
+  // Issues the TMA loads of the worker's tile j (cursor c) into stage st; lane 0 records in
+  // `valid` (bit st) whether the tile's block id was inside the pool.  Whole warp calls it.
+  uint32_t valid = 0;
+  auto issue = [&](const Tile& c, int j, int st) {
+    if (j % 32 == 0 && j > 0) {
+      bid_cur = bid_nxt;
+      bid_nxt = load_window(j / 32 + 1);
+    }
+    const int pb = __shfl_sync(0xffffffffu, bid_cur, j % 32);
     if (lane != 0) return;
-    const int pb = p.block_tables[int64_t(c.s) * p.max_blocks + c.b];
     uint64_t* bar = &bars[warp][st];
     if (pb < 0 || pb >= p.num_blocks) {
       set_error(p.err, PKV_DEVERR_BLOCK_ID);
+      valid &= ~(1u << st);
       mbar_arrive(bar);                      // completes the phase without data
       return;
     }
+    valid |= 1u << st;
     mbar_arrive_expect_tx(bar, C::kStageBytes);
     const int y = int((int64_t(pb) * Hkv + c.h) * kBS);
     uint8_t* kdst = my_stages + st * C::kStageBytes;
@@ -273,7 +300,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   Tile pc = locate(t_begin);                 // producer cursor, kStages tiles ahead
   for (int i = 0; i < min(n, kStages); ++i) {
-    issue(pc, i);
+    issue(pc, i, i);
     advance(pc);
   }
   Tile tl = locate(t_begin);                 // consumer cursor
@@ -287,7 +314,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
   for (int i = 0; i < n; ++i, advance(tl)) {
     const int st = i % kStages;
-    const bool piece_start = i == 0 || tl.b == 0 || (PB && tl.b % PB == 0);
+    const bool piece_start = i == 0 || tl.b == 0;
     if (piece_start) {
       piece_b0 = tl.b;
       m0 = m1 = -INFINITY;
@@ -312,7 +339,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       }
     }
 
-    const int pb = p.block_tables[int64_t(tl.s) * p.max_blocks + tl.b];
     if (!mbar_wait(&bars[warp][st], uint32_t(i / kStages) & 1u)) {
       // Give up: report, then wait (bounded) for this warp's loads still in flight.
       if (lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -320,7 +346,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       return;
     }
 
-    const int nv = (pb < 0 || pb >= p.num_blocks) ? 0 : min(kBS, tl.len - tl.b * kBS);
+    const bool ok = (__shfl_sync(0xffffffffu, valid, 0) >> st) & 1u;
+    const int nv = ok ? min(kBS, tl.len - tl.b * kBS) : 0;
     if (nv > 0) {
       const uint32_t kbase = smem_u32(my_stages + st * C::kStageBytes);
       const uint32_t vbase = kbase + C::kTileBytes;
@@ -373,6 +400,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const bool grew = mn0 > m0 || mn1 > m1;
       const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
@@ -380,9 +408,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       const float p2 = fast_exp2(x[2] - mn0), p3 = fast_exp2(x[3] - mn1);
       l0 = l0 * al0 + p0 + p2;
       l1 = l1 * al1 + p1 + p3;
+      if (__any_sync(0xffffffffu, grew)) {     // the running max moved: rescale O
 #pragma unroll
-      for (int mt = 0; mt < C::kMTiles; ++mt) {
-        o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+        for (int mt = 0; mt < C::kMTiles; ++mt) {
+          o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
+        }
       }
       // P^T as the B operand: lane (g, t) needs head g, tokens {2t, 2t+1} and {2t+8, 2t+9}.
       constexpr bool kPB = C::kBF16;
@@ -425,21 +455,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
           const int chunk = 2 * mt + (mi & 1);
           uint32_t a[4];
           ldsm_x4_trans(vbase + (chunk >> 3) * 2048 + swz128(row, chunk & 7), a[0], a[1], a[2], a[3]);
-          a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
+          if (nv < kBS) { a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89; }
           mma16816<C::kBF16>(o[mt], a, pb0, pb1);
         }
       }
     }
 
-    // Release the stage and refill it with the tile kStages ahead.
+    // Release the stage and refill it with the tile kStages ahead.  Every lane's shared
+    // loads of this stage have returned (their values fed the MMAs above), so the TMA
+    // write cannot overtake them.
     __syncwarp();
-    fence_proxy_async_smem();
     if (i + kStages < n) {
-      issue(pc, st);
+      issue(pc, i + kStages, st);
       advance(pc);
     }
 
-    const bool piece_end = i == n - 1 || tl.b + 1 == tl.nb || (PB && (tl.b + 1) % PB == 0);
+    const bool piece_end = i == n - 1 || tl.b + 1 == tl.nb;
     if (!piece_end) continue;
 
     // ---- finish the piece [piece_b0, tl.b] of segment (s, h) -----------------------------
@@ -452,7 +483,26 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const float vs = KV == KV_E4M3 ? p.v_scale[tl.h] : 1.f;
     const int h0 = 2 * tq, h1 = 2 * tq + 1;
     const int Hq = Hkv * G;
+    const int seg = tl.s * Hkv + tl.h;
+    const int64_t seg_t0 = int64_t(Hkv) * cum_nb[tl.s] + int64_t(tl.h) * tl.nb;
+    const int64_t piece_t0 = seg_t0 + piece_b0;
     const bool complete = piece_b0 == 0 && tl.b + 1 == tl.nb;
+    if (piece_b0 == 0 && lane == 0) {
+      // This worker holds the segment's first tile: describe the segment's pieces for the
+      // merge kernel.  Workers w .. w1 cover it, one piece each; worker w's piece is its
+      // first (slot 2w) if the segment starts its range, else its second (slot 2w + 1).
+      int npieces = 1;
+      if (!complete) {
+        const int64_t last = seg_t0 + tl.nb - 1;
+        auto range_begin = [&](int64_t wi) -> int64_t { return PB ? unit_tile(start_of(wi)) : start_of(wi); };
+        const int64_t guess = last * W / T;
+        int wi = int(guess < W - 1 ? guess : W - 1);
+        while (wi > 0 && range_begin(wi) > last) --wi;
+        while (wi + 1 < W && range_begin(wi + 1) <= last) ++wi;
+        npieces = wi - w + 1;
+      }
+      p.seg_desc[seg] = make_int4(w, npieces, piece_t0 == t_begin ? 0 : 1, 0);
+    }
     if (complete) {
       const float inv0 = ls0 > 0.f ? vs / ls0 : 0.f, inv1 = ls1 > 0.f ? vs / ls1 : 0.f;
       const int64_t base = (int64_t(tl.s) * Hq + int64_t(tl.h) * G) * D;
@@ -467,138 +517,159 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       }
       continue;
     }
-
-    // Partial: slot, pieces of this segment, then arrive on its counter.
-    const int seg = tl.s * Hkv + tl.h;
-    const int64_t seg_t0 = int64_t(Hkv) * cum_nb[tl.s] + int64_t(tl.h) * tl.nb;
-    const int64_t seg_t1 = seg_t0 + tl.nb;
-    int npieces;
-    int64_t slot;
-    int64_t slot0 = 0;     // partition mode: first unit of the segment
-    int w0 = 0;            // balanced mode: first worker of the segment
-    bool w0_first = false;
-    if (PB) {
-      const int np = cum_np[tl.s + 1] - cum_np[tl.s];
-      slot0 = int64_t(Hkv) * cum_np[tl.s] + int64_t(tl.h) * np;
-      npieces = np;
-      slot = slot0 + piece_b0 / PB;
-    } else {
-      auto worker_of = [&](int64_t tt) {
-        int64_t wi = tt * W / nunits;
-        while (wi + 1 < W && start_of(wi + 1) <= tt) ++wi;
-        while (start_of(wi) > tt) --wi;
-        return int(wi);
-      };
-      w0 = worker_of(seg_t0);
-      const int w1 = worker_of(seg_t1 - 1);
-      npieces = w1 - w0 + 1;
-      w0_first = seg_t0 == start_of(w0);
-      slot = (w == w0 && !w0_first) ? 2 * int64_t(w) + 1 : 2 * int64_t(w);
-    }
-    {
-      float* po = p.po + slot * G * D;
+    // Partial piece: (running max, sum of exponentials, unnormalised output) per head.
+    const int64_t slot = 2 * int64_t(w) + (piece_t0 == t_begin ? 0 : 1);
+    float* po = p.po + slot * G * D;
 #pragma unroll
-      for (int mt = 0; mt < C::kMTiles; ++mt) {
+    for (int mt = 0; mt < C::kMTiles; ++mt) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int d = out_dim<KV>(mt, r, gq);
-          if (h0 < G) po[h0 * D + d] = o[mt][2 * r] * vs;
-          if (h1 < G) po[h1 * D + d] = o[mt][2 * r + 1] * vs;
-        }
-      }
-      if (gq == 0) {
-        if (h0 < G) p.ml[slot * G + h0] = make_float2(m0, ls0);
-        if (h1 < G) p.ml[slot * G + h1] = make_float2(m1, ls1);
+      for (int r = 0; r < 2; ++r) {
+        const int d = out_dim<KV>(mt, r, gq);
+        if (h0 < G) po[h0 * D + d] = o[mt][2 * r] * vs;
+        if (h1 < G) po[h1 * D + d] = o[mt][2 * r + 1] * vs;
       }
     }
-    __threadfence();
-    __syncwarp();
-    int old = 0;
-    if (lane == 0) old = atomicAdd(p.counters + seg, 1);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != npieces - 1) continue;
-
-    // Last piece to arrive: merge every piece of the segment by log-sum-exp.
-    __threadfence();
-    constexpr int kVec = D / 32;   // head_dim elements per lane
-    for (int hh = 0; hh < G; ++hh) {
-      auto slot_of = [&](int k) -> int64_t {
-        if (PB) return slot0 + k;
-        return (k == 0 && !w0_first) ? 2 * int64_t(w0) + 1 : 2 * int64_t(w0 + k);
-      };
-      float M = -INFINITY;
-      for (int k = lane; k < npieces; k += 32) M = fmaxf(M, __ldcg(&p.ml[slot_of(k) * G + hh]).x);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      float acc[kVec];
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
-      float den = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll 4
-        for (int k = 0; k < npieces; ++k) {
-          const int64_t sk = slot_of(k);
-          const float2 ml = __ldcg(&p.ml[sk * G + hh]);
-          const float wk = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-          den += wk * ml.y;
-          const float* src = p.po + (sk * G + hh) * D + lane * kVec;
-          if constexpr (kVec == 4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-            acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
-          } else {
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-            acc[0] += wk * v.x; acc[1] += wk * v.y;
-          }
-        }
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      const int64_t obase = (int64_t(tl.s) * Hq + int64_t(tl.h) * G + hh) * D + lane * kVec;
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) store_out<QT>(p.out, obase + e, acc[e] * inv);
+    if (gq == 0) {
+      if (h0 < G) p.ml[slot * G + h0] = make_float2(m0, ls0);
+      if (h1 < G) p.ml[slot * G + h1] = make_float2(m1, ls1);
     }
-    if (lane == 0) p.counters[seg] = 0;
   }
+}
+
+struct MergeParams {
+  void* out;
+  const int4* seg_desc;
+  const float2* ml;
+  const float* po;
+  int num_segments;       // num_seqs * num_kv_heads
+  int group;
+};
+
+constexpr int kMergeWarps = 8;
+
+// Split-KV merge: one warp per (sequence, query head) whose segment was split.  With
+// M = max_k m_k over the pieces k,  out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k.
+template <int QT, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32) split_kv_merge_kernel(const MergeParams p) {
+  griddep_wait();                            // the decode kernel's partials are complete
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int64_t item = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (item >= int64_t(p.num_segments) * G) return;
+  const int seg = int(item / G), hh = int(item % G);
+  const int4 d = p.seg_desc[seg];
+  const int w0 = d.x, npieces = d.y;
+  if (npieces <= 1) return;
+  auto slot_of = [&](int k) -> int64_t { return k == 0 ? 2 * int64_t(w0) + d.z : 2 * int64_t(w0 + k); };
+  float M = -INFINITY;
+  for (int k = lane; k < npieces; k += 32) M = fmaxf(M, p.ml[slot_of(k) * G + hh].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  constexpr int kVec = D / 32;
+  float acc[kVec];
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
+  float den = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll 8
+    for (int k = 0; k < npieces; ++k) {
+      const int64_t sk = slot_of(k);
+      const float2 ml = p.ml[sk * G + hh];
+      const float wk = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
+      den += wk * ml.y;
+      const float* src = p.po + (sk * G + hh) * D + lane * kVec;
+      if constexpr (kVec == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += wk * v.x; acc[1] += wk * v.y;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const int64_t obase = (int64_t(seg) * G + hh) * D + lane * kVec;   // out[s][h * G + hh][:]
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) store_out<QT>(p.out, obase + e, acc[e] * inv);
 }
 
 // ---------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------
 struct Layout {
-  size_t counters = 0, ml = 0, po = 0, total = 0;
+  size_t desc = 0, ml = 0, po = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-int64_t num_slots(int num_seqs, int num_kv_heads, int max_context_len, int part_blocks, int workers) {
-  if (part_blocks == 0) return 2 * int64_t(workers);
-  const int64_t nb = (int64_t(std::max(max_context_len, 0)) + kBS - 1) / kBS;
-  return int64_t(num_seqs) * num_kv_heads * ((nb + part_blocks - 1) / part_blocks);
-}
+int64_t num_slots(int workers) { return 2 * int64_t(workers); }
 
 Layout layout(int num_seqs, int num_kv_heads, int group, int head_dim, int64_t slots) {
   Layout l;
-  l.counters = 0;
-  l.ml = align256(sizeof(int) * size_t(num_seqs) * num_kv_heads);
+  l.desc = 0;
+  l.ml = align256(sizeof(int4) * size_t(num_seqs) * num_kv_heads);
   l.po = l.ml + align256(sizeof(float2) * size_t(slots) * group);
   l.total = l.po + align256(sizeof(float) * size_t(slots) * group * head_dim);
   return l;
 }
 
-template <int KV, int D>
+constexpr size_t kSmemLimit = 227 * 1024;
+
+template <int KV, int D, int NW, int NS>
 size_t smem_bytes(int num_seqs) {
-  return 1024 + size_t(kWarps) * kStages * Cfg<KV, D>::kStageBytes + 2 * sizeof(int) * size_t(num_seqs + 1);
+  return 1024 + size_t(NW) * NS * Cfg<KV, D>::kStageBytes + 2 * sizeof(int) * size_t(num_seqs + 1);
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel on the stream runs, and waits for it in griddep_wait().
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <int KV, int QT, int D, int NW, int NS>
+pkv_status launch_cfg(DecodeParams prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                      cudaStream_t stream) {
+  auto kern = paged_decode_kernel<KV, QT, D, NW, NS>;
+  const size_t smem = smem_bytes<KV, D, NW, NS>(prm.num_seqs);
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  prm.num_workers = grid * NW;
+  if (launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, prm) != cudaSuccess) return PKV_ERR_CUDA;
+  MergeParams mp;
+  mp.out = prm.out;
+  mp.seg_desc = prm.seg_desc;
+  mp.ml = prm.ml;
+  mp.po = prm.po;
+  mp.num_segments = prm.num_seqs * prm.num_kv_heads;
+  mp.group = prm.group;
+  const int64_t items = int64_t(mp.num_segments) * mp.group;
+  const int mgrid = int((items + kMergeWarps - 1) / kMergeWarps);
+  if (launch_pdl(split_kv_merge_kernel<QT, D>, dim3(mgrid), dim3(kMergeWarps * 32), 0, stream, mp) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+// 12 worker warps with 2 stages each when the per-sequence prefix arrays fit next to the
+// stages, else 4 warps with 2 stages (very large batches).
 template <int KV, int QT, int D>
 pkv_status launch(const DecodeParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                   cudaStream_t stream) {
-  auto kern = paged_decode_kernel<KV, QT, D>;
-  const size_t smem = smem_bytes<KV, D>(prm.num_seqs);
-  if (smem > 227 * 1024) return PKV_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  kern<<<grid, kWarps * 32, smem, stream>>>(tk, tv, prm);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  if (smem_bytes<KV, D, kMaxWarps, 2>(prm.num_seqs) <= kSmemLimit)
+    return launch_cfg<KV, QT, D, kMaxWarps, 2>(prm, tk, tv, grid, stream);
+  if (smem_bytes<KV, D, 4, 2>(prm.num_seqs) <= kSmemLimit) return launch_cfg<KV, QT, D, 4, 2>(prm, tk, tv, grid, stream);
+  return PKV_ERR_UNSUPPORTED;
 }
 
 int decode_grid() { return std::max(1, num_sms()); }
@@ -615,8 +686,8 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
       partition_size % kBS)
     return 0;
   const int group = num_heads / num_kv_heads;
-  const int workers = decode_grid() * kWarps;
-  const int64_t slots = num_slots(num_seqs, num_kv_heads, max_context_len, partition_size / kBS, workers);
+  const int workers = decode_grid() * kMaxWarps;
+  const int64_t slots = num_slots(workers);
   return layout(num_seqs, num_kv_heads, group, head_dim, slots).total;
 }
 
@@ -649,7 +720,7 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
 
   const int grid = decode_grid();
   const int part_blocks = partition_size / kBS;
-  const int64_t slots = num_slots(num_seqs, cache->num_kv_heads, max_context_len, part_blocks, grid * kWarps);
+  const int64_t slots = num_slots(grid * kMaxWarps);
   const Layout lay = layout(num_seqs, cache->num_kv_heads, group, D, slots);
   if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   unsigned* err = error_word_ptr();
@@ -681,9 +752,8 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   prm.max_len = int(std::min<int64_t>(int64_t(max_blocks_per_seq) * kBS, max_context_len));
   prm.num_blocks = cache->num_blocks;
   prm.part_blocks = part_blocks;
-  prm.num_workers = grid * kWarps;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  prm.counters = reinterpret_cast<int*>(ws + lay.counters);
+  prm.seg_desc = reinterpret_cast<int4*>(ws + lay.desc);
   prm.ml = reinterpret_cast<float2*>(ws + lay.ml);
   prm.po = reinterpret_cast<float*>(ws + lay.po);
   prm.err = err;

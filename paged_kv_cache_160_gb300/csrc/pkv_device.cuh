@@ -77,6 +77,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while its predecessor runs; griddep_wait() blocks until the predecessor has
+// completed and its memory is visible.  Both are no-ops for ordinary launches.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------
 // TMA (tensor memory accelerator) tile loads
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
