@@ -157,6 +157,31 @@ PKV_API pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype,
                             pkv_stream_t stream);
 
 /*
+ * paged_decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that must not allocate at decode
+ * time: a plain C host without a device allocator of its own for scratch space, or a
+ * serving loop that may not call cudaMalloc on its hot path because cudaMalloc can
+ * synchronise the whole device.  Same arguments and results as pkv_paged_decode, minus the
+ * workspace: the library keeps one fixed scratch array of pkv_noalloc_scratch_bytes()
+ * (24 MiB) on every device that loads it, resident until the process exits.  A call that
+ * needs more scratch than that (per pkv_decode_workspace_bytes) returns PKV_ERR_WORKSPACE
+ * and enqueues nothing.  No call allocates, frees or clears device memory: each call
+ * rewrites the parts of the array it later reads, so leftovers of earlier calls do no
+ * harm.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture.  Every call on a device shares the one array, so calls whose kernels
+ * may overlap on the GPU (different streams with no ordering between them) race and
+ * corrupt each other's results: keep them on one stream or order them with events.
+ */
+PKV_API size_t pkv_noalloc_scratch_bytes(void);
+PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype, int num_seqs,
+                                            int num_heads, const void* k_cache, const void* v_cache,
+                                            const pkv_cache_desc* cache, const int32_t* block_tables,
+                                            int max_blocks_per_seq, const int32_t* context_lens,
+                                            int max_context_len, float scale, int partition_size,
+                                            pkv_stream_t stream);
+
+/*
  * paged_prefill_chunk: causal attention of prefill chunks over their paged history
  * (Lecture 33 §4.2: a chunk attends the earlier chunks' cached KV, masked causally).
  * Chunk c holds query rows cu_q_lens[c] .. cu_q_lens[c+1]-1; row r of the chunk is at

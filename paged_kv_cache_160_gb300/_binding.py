@@ -57,6 +57,12 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_decode.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                      POINTER(CacheDesc), c_void_p, c_int, c_void_p, c_int, c_float, c_int,
                                      c_void_p, c_size_t, c_void_p]
+    lib.pkv_noalloc_scratch_bytes.restype = c_size_t
+    lib.pkv_noalloc_scratch_bytes.argtypes = []
+    lib.pkv_paged_decode_noalloc.restype = S
+    lib.pkv_paged_decode_noalloc.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
+                                             POINTER(CacheDesc), c_void_p, c_int, c_void_p, c_int, c_float, c_int,
+                                             c_void_p]
     lib.pkv_paged_prefill_chunk.restype = S
     lib.pkv_paged_prefill_chunk.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
                                             c_int, c_void_p, c_void_p, POINTER(CacheDesc), c_void_p, c_int,
@@ -184,6 +190,22 @@ def pkv_paged_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, 
                                 int(partition_size), _dev(workspace, "workspace"),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "pkv_paged_decode")
+
+
+def pkv_noalloc_scratch_bytes() -> int:
+    return int(lib.pkv_noalloc_scratch_bytes())
+
+
+def pkv_paged_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             desc: CacheDesc, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                             max_context_len: int, scale: float, partition_size: int, stream=None) -> None:
+    """pkv_paged_decode with the library's own fixed scratch array instead of a workspace."""
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    _check(lib.pkv_paged_decode_noalloc(_dev(out, "out"), _dev(q, "q"), pkv_dtype_of(q), q.shape[0], q.shape[1],
+                                        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                        _dev(block_tables, "block_tables"), block_tables.shape[1],
+                                        _dev(context_lens, "context_lens"), int(max_context_len), float(scale),
+                                        int(partition_size), _stream(stream)), "pkv_paged_decode_noalloc")
 
 
 def pkv_paged_prefill_chunk(out: torch.Tensor, q: torch.Tensor, cu_q_lens: torch.Tensor, q_start_pos: torch.Tensor,
