@@ -88,7 +88,7 @@ def test_long_splitkv_e4m3_sampled(part):
 
 def test_mixed_step_decode_and_copies():
     case = synth.mixed_config()
-    _check_case(case, prefill_rows=[0, 1, 255, 511], prefill_heads=[0, 6, 27], run_prefill=False)
+    _check_case(case, prefill_rows=[0, 1, 255, 511], prefill_heads=[0, 6, 27])
 
 
 # ---------------------------------------------------------------------------------------

@@ -1,0 +1,120 @@
+"""GPU parity of paged_prefill_chunk (tcgen05 path) against the fp64 oracle.
+
+Each case builds a paged pool holding, per chunk, a cached prefix followed by the chunk's
+own K/V (written on the host by plain indexing), runs the chunks in one launch (varlen
+via cu_q_lens) and compares every output row with the oracle's causal chunk attention.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from tests.harness import TOL, codes, q_f64
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+
+
+def _case(seed, chunks, hq, hkv, dtype, nan_fill=False, D=128, bs=16):
+    g = torch.Generator().manual_seed(seed)
+    need = [-(-(p + n) // bs) for p, n in chunks]
+    nb = sum(need) + 5
+    perm = torch.randperm(nb, generator=g).tolist()
+    tables, pos = [], 0
+    for k in need:
+        tables.append(perm[pos:pos + k]); pos += k
+    mb = max(need)
+    k_pool = torch.randn((nb, hkv, bs, D), generator=g).to(DT[dtype])
+    v_pool = torch.randn((nb, hkv, bs, D), generator=g).to(DT[dtype])
+    if nan_fill:
+        valid = torch.zeros((nb, bs), dtype=torch.bool)
+        for t, (p, n) in zip(tables, chunks):
+            for j in range(p + n):
+                valid[t[j // bs], j % bs] = True
+        m = (~valid).view(nb, 1, bs, 1).expand_as(k_pool)
+        k_pool[m] = float("nan")
+        v_pool[m] = float("nan")
+    total = sum(n for _, n in chunks)
+    q = torch.randn((total, hq, D), generator=g).to(DT[dtype])
+    cu = [0]
+    for _, n in chunks:
+        cu.append(cu[-1] + n)
+    tab = [t + [-1] * (mb - len(t)) for t in tables]
+    return dict(k=k_pool, v=v_pool, q=q, cu=cu, starts=[p for p, _ in chunks], tables=tab, dtype=dtype,
+                hq=hq, hkv=hkv, max_q=max(n for _, n in chunks), chunks=chunks)
+
+
+def _run(c):
+    import paged_kv_cache_160_gb300 as pkv
+    dev = torch.device("cuda")
+    kc, vc = c["k"].to(dev), c["v"].to(dev)
+    desc = pkv.cache_desc(kc)
+    q = c["q"].to(dev)
+    out = torch.full_like(q, float("nan"))
+    pkv.pkv_get_device_error()
+    pkv.pkv_paged_prefill_chunk(out, q, torch.tensor(c["cu"], dtype=torch.int32, device=dev),
+                                torch.tensor(c["starts"], dtype=torch.int32, device=dev), c["max_q"], kc, vc, desc,
+                                torch.tensor(c["tables"], dtype=torch.int32, device=dev), 1 / math.sqrt(128))
+    err = pkv.pkv_get_device_error()
+    return out.cpu(), err
+
+
+def _check(c, rows_per_chunk=None):
+    from oracle.paged_attention import prefill_chunk_attention
+    out, err = _run(c)
+    assert err == 0, f"device error {err:#x}"
+    kcodes, vcodes = codes(c["k"]), codes(c["v"])
+    worst = 0.0
+    for i, (p, n) in enumerate(c["chunks"]):
+        lo, hi = c["cu"][i], c["cu"][i + 1]
+        rows = None if rows_per_chunk is None else [r for r in rows_per_chunk if r < n]
+        ref = prefill_chunk_attention(q_f64(c["q"][lo:hi]), kcodes, vcodes, c["dtype"], c["tables"][i], p,
+                                      1 / math.sqrt(128), rows=rows)
+        got = out[lo:hi].to(torch.float64).numpy()
+        mask = ~np.isnan(ref)
+        d = np.abs(got[mask] - ref[mask])
+        assert not np.isnan(d).any(), f"NaN in chunk {i}"
+        worst = max(worst, float(d.max()))
+    assert worst <= TOL[c["dtype"]], f"max abs err {worst:.3e}"
+    return worst
+
+
+def test_single_chunk_no_prefix_bf16():
+    _check(_case(1, [(0, 128)], 4, 4, "bf16"))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_varlen_chunks_ragged(dtype):
+    # prefixes not aligned to 128 or 16, q_len not multiples of 128, one chunk of 1 token
+    _check(_case(2, [(37, 200), (0, 5), (300, 129), (1000, 1), (128, 256)], 8, 2, dtype))
+
+
+def test_gqa7_long_prefix():
+    _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
+
+
+def test_nan_in_unused_rows_never_reaches_output():
+    _check(_case(4, [(5, 40), (77, 100)], 4, 1, "bf16", nan_fill=True))
+
+
+def test_mixed_workload_chunk():
+    """The mixed step's 512-token chunk at positions 3584..4095, after kv_write, via the harness."""
+    import synth
+    from tests.harness import device_run, max_abs_err, oracle_plan, oracle_run, product_plan
+    case = synth.mixed_config()
+    pp = product_plan(case)
+    assert pp == oracle_plan(case)
+    dev = device_run(case, pp, keep_intermediate=False)
+    assert dev.device_error == 0
+    ref = oracle_run(case, pp, decode_rows=[(0, 0)], prefill_rows=[0, 1, 100, 255, 256, 400, 511],
+                     prefill_heads=[0, 6, 7, 20, 27])
+    err = max_abs_err(dev.prefill, ref.prefill)
+    assert err <= TOL["bf16"], err
