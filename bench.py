@@ -7,8 +7,9 @@ One step = plan the step on the host block manager (done once; its cost is repor
 separately), kv_write of the 64 new tokens, then paged_decode over every sequence's
 L + 1 tokens (one launch: split-KV and merge).
 
-Timing: CUDA events on the launching stream.  The kernels of a step are captured once
-per pool copy into CUDA graphs; the timed loop replays them.  Every step uses the next of
+Timing: CUDA events on the launching stream.  The K timed steps are captured into one
+CUDA graph and replayed once between two events.  The decode kernel's own average duration
+(split + merge, for its roofline) comes from a second graph of K decodes timed the same way.  Every step uses the next of
 R pool copies whose combined size is above 3x the L2 size, so no step finds its K/V in L2.
 `value` is device-resident throughput; `e2e` adds, every step, the pinned host->device
 copies of the step's inputs (q, new K/V, slots, tables, lengths) and the device->host copy
@@ -46,7 +47,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes per paged_decode launch on this workload from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel source with
 # this hash; when the source changes, traffic is reported as null until re-measured.
-TRAFFIC = {"source_sha1": None, "bytes_per_launch": None}
+TRAFFIC = {"source_sha1": "1be57afd78389a70cc8243eaa99ed48069e3ae28", "bytes_per_launch": 154050048}
 
 
 def _src_hash() -> str:
@@ -62,6 +63,30 @@ def _peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def _bf16_peak() -> float:
+    """Measured dense bf16 TFLOP/s (burst: the prefill kernel is timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return float(json.load(open(path))["bf16_tflops"])
+    return 1900.0
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (the slowest rank defines the timed region)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank: int, ms_per_step: float, world: int) -> float:
+    """Whole-job GB/s: every rank runs its own replica of the step (weak scaling)."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 def _dist():
@@ -199,54 +224,64 @@ def run_gpu(args):
             decode(r)
     stream.synchronize()
     assert pkv.pkv_get_device_error(stream) == 0
-    g_write, g_dec = [], []
-    for r in range(R):
-        gw, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gw, stream=stream, capture_error_mode="thread_local"):
-            write(r)
-        with torch.cuda.graph(gd, stream=stream, capture_error_mode="thread_local"):
-            decode(r)
-        g_write.append(gw)
-        g_dec.append(gd)
-    torch.cuda.synchronize(dev)
-
     K, W = args.steps, args.warmup
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def barrier():
         if ws_n > 1:
             import torch.distributed as dist
             dist.barrier()
 
+    # The timed loop is one CUDA graph of K steps (each: kv_write -> decode -> split-KV merge,
+    # the last two launched as programmatic dependents), rotating over the pool copies.  The
+    # decode kernel's own average duration (split + merge, for its roofline) is timed the same
+    # way on a graph of K decodes alone; event nodes between kernels would break the
+    # programmatic launches and inflate it.
+    def capture(n_steps, first, with_write=True):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for k in range(n_steps):
+                r = (first + k) % R
+                if with_write:
+                    write(r)
+                decode(r)
+        return g
+
+    g_warm = capture(W, 0)
+    g_timed = capture(K, W)
+    g_dec_warm = capture(W, 0, with_write=False)
+    g_dec = capture(K, W, with_write=False)
+    g_step = []                                          # single steps, for the e2e loop
+    for r in range(R):
+        gs = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gs, stream=stream, capture_error_mode="thread_local"):
+            write(r)
+            decode(r)
+        g_step.append(gs)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
     with torch.cuda.stream(stream):
-        for k in range(W):
-            g_write[k % R].replay()
-            g_dec[k % R].replay()
+        g_warm.replay()
     stream.synchronize()
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             start.record(stream)
-            for k in range(K):
-                r = (W + k) % R
-                g_write[r].replay()
-                ev_a[k].record(stream)
-                g_dec[r].replay()
-                ev_b[k].record(stream)
+            g_timed.replay()
             end.record(stream)
         stream.synchronize()
-    barrier()
-    torch.cuda.synchronize(dev)
-    elapsed_ms = start.elapsed_time(end)
-    dec_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
-    if ws_n > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            g_dec_warm.replay()
+            d_start.record(stream)
+            g_dec.replay()
+            d_end.record(stream)
+        stream.synchronize()
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev)
+    dec_avg_ms = d_start.elapsed_time(d_end) / K
     assert pkv.pkv_get_device_error(stream) == 0
 
     # ---- end to end: host buffers, copies inside the timed region -----------------------
@@ -272,24 +307,18 @@ def run_gpu(args):
             slots.copy_(h_slots, non_blocking=True)
             tables.copy_(h_tables, non_blocking=True)
             lens.copy_(h_lens, non_blocking=True)
-            g_write[r].replay()
-            g_dec[r].replay()
+            g_step[r].replay()
             h_out.copy_(out, non_blocking=True)
         e_end.record(stream)
     stream.synchronize()
     barrier()
-    e2e_ms = e_start.elapsed_time(e_end)
-    if ws_n > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     assert torch.equal(h_out.to(dev), out)
+    pf_ms, pf_flops = prefill_measure(dev)
 
     peak, peak_kind = _peaks()
     ms_per_step = elapsed_ms / K
-    value = ws_n * step_bytes / (ms_per_step * 1e-3) / 1e9
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    value = aggregate_gbs(step_bytes, ms_per_step, ws_n)
     achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha1"] == _src_hash() else None
     line = {
@@ -308,7 +337,8 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "num_seqs": case.num_seqs, "attended_tokens": tokens,
                    "step_bytes": step_bytes, "decode_bytes": decode_bytes, "kv_write_bytes": write_bytes,
                    "pool_copies": R, "l2": f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB > 3x L2)",
-                   "launch": "CUDA graph replay per kernel", "partition_size": part,
+                   "launch": "one CUDA graph of K steps (kv_write, decode, merge per step; programmatic dependent launches)",
+                   "partition_size": part,
                    "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
         "seq_tokens_per_s": round(ws_n * tokens / (ms_per_step * 1e-3), 1),
         "pct_of_nominal_8tbs": round(100 * value / ws_n / NOMINAL_HBM_GBS, 2),
@@ -319,10 +349,15 @@ def run_gpu(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
-        "e2e": {"value": round(ws_n * step_bytes / (e2e_ms / K * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(aggregate_gbs(step_bytes, e2e_ms / K, ws_n), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "prefill_chunk": {"workload": "mixed-step chunk: 512 causal rows at 3584..4095, 28/4 heads, bf16",
+                          "bound": "tensor", "achieved": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1),
+                          "peak": _bf16_peak(), "unit": "TFLOP/s",
+                          "frac": round(pf_flops / (pf_ms * 1e-3) / 1e12 / _bf16_peak(), 4),
+                          "avg_launch_ms": round(pf_ms, 5), "flops_per_launch": pf_flops},
         "host_plan_us": round(host_plan_us, 1),
-        "gpu_launches": 2 * K,
+        "gpu_launches": 3 * K,                       # kv_write, decode, merge per timed step
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -331,6 +366,54 @@ def run_gpu(args):
     if ws_n > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def prefill_measure(dev, iters: int = 30):
+    """paged_prefill_chunk on the mixed workload's chunk: 512 causal rows at positions
+    3584..4095 over the sequence's paged cache, 28/4 heads, bf16.  CUDA-graph replays timed
+    with events; FLOPs = 4 * head_dim * (attended query-key pairs) * heads."""
+    import torch
+    import paged_kv_cache_160_gb300 as pkv
+    import synth
+    from tests.harness import product_plan
+    case = synth.mixed_config()
+    plan = product_plan(case)
+    ch = case.chunk
+    kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+    desc = pkv.cache_desc(kc)
+    pkv.pkv_kv_write(ch.k_new.to(dev), ch.v_new.to(dev), torch.tensor(plan.chunk_slots, dtype=torch.int64, device=dev),
+                     kc, vc, desc)
+    q = ch.q.to(dev)
+    out = torch.empty_like(q)
+    cu = torch.tensor([0, ch.q_len], dtype=torch.int32, device=dev)
+    st0 = torch.tensor([ch.prefix_len], dtype=torch.int32, device=dev)
+    tab = torch.tensor([plan.chunk_table], dtype=torch.int32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def run():
+        pkv.pkv_paged_prefill_chunk(out, q, cu, st0, ch.q_len, kc, vc, desc, tab, case.scale)
+
+    with torch.cuda.stream(s):
+        run()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+        run()
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.replay()
+        for k in range(iters):
+            ea[k].record(s)
+            g.replay()
+            eb[k].record(s)
+    s.synchronize()
+    assert pkv.pkv_get_device_error(s) == 0
+    ms = sum(a.elapsed_time(b) for a, b in zip(ea, eb)) / iters
+    pairs = sum(ch.prefix_len + r + 1 for r in range(ch.q_len))
+    flops = 4 * case.head_dim * pairs * case.num_heads
+    return ms, flops
 
 
 def _oracle_step(case, plan, seqs):

@@ -49,7 +49,7 @@ typedef struct CUstream_st* pkv_stream_t;
 typedef enum {
   PKV_OK = 0,
   PKV_ERR_INVALID_ARG = 1,   /* a host-visible argument is out of range / misaligned */
-  PKV_ERR_UNSUPPORTED = 2,   /* valid, but this build has no kernel for it (e.g. head_dim 96) */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid, but the library has no kernel for it (e.g. head_dim 96) */
   PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than pkv_decode_workspace_bytes() */
   PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   PKV_ERR_NO_BLOCKS = 5,     /* block manager: the free-block queue cannot cover the request */
@@ -148,6 +148,12 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_k
  * Supported: kv f16/bf16 with the same q dtype, or e4m3 kv with f16/bf16 q (the e4m3
  * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16;
  * num_heads / num_kv_heads in 1..8.
+ * Launch order: the decode kernel is launched as a programmatic dependent of the previous
+ * kernel on `stream`.  If that kernel allows early dependent launch (pkv_kv_write does), the
+ * decode kernel may already read context_lens and block_tables while it still runs; q, the
+ * caches, out and the workspace are touched only after it has completed.  So the kernel
+ * right before a decode call must not write context_lens or block_tables unless it leaves
+ * dependent launch at its default (wait for completion).
  */
 PKV_API pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
                             const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,

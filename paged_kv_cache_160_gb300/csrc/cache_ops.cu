@@ -122,10 +122,12 @@ __global__ void __launch_bounds__(kThreads) copy_blocks_kernel(uint4* __restrict
   for (int64_t i = threadIdx.x; i < chunks; i += blockDim.x) d[i] = s[i];
 }
 
+// One 16-byte chunk per thread: these kernels are latency-bound at serving sizes, so every
+// thread should issue its loads once rather than loop.
 int grid_for(int64_t work) {
-  const int64_t per = kThreads * 4;
+  const int64_t per = kThreads;
   int64_t g = (work + per - 1) / per;
-  const int cap = num_sms() > 0 ? num_sms() * 8 : 1024;
+  const int cap = num_sms() > 0 ? num_sms() * 64 : 8192;
   if (g > cap) g = cap;
   return g < 1 ? 1 : int(g);
 }

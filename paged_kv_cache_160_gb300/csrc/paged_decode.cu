@@ -189,25 +189,28 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
   }
   __syncthreads();
-  // Everything above reads only lengths; from here on the kernel reads the cache and
-  // writes outputs, so it waits for the preceding kernel (a KV write) to finish.
-  griddep_wait();
-  griddep_launch_dependents();
 
   // Sequences with nothing to attend produce zeros (their tiles never exist).
-  for (int s = blockIdx.x; s < S; s += gridDim.x) {
-    if (cum_nb[s + 1] != cum_nb[s]) continue;
-    const int n = Hkv * G * D;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) store_out<QT>(p.out, int64_t(s) * n + e, 0.f);
-    if (threadIdx.x < Hkv) p.seg_desc[s * Hkv + threadIdx.x] = make_int4(0, 0, 0, 0);
-  }
+  auto zero_empty = [&]() {
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+      if (cum_nb[s + 1] != cum_nb[s]) continue;
+      const int n = Hkv * G * D;
+      for (int e = threadIdx.x; e < n; e += blockDim.x) store_out<QT>(p.out, int64_t(s) * n + e, 0.f);
+      if (threadIdx.x < Hkv) p.seg_desc[s * Hkv + threadIdx.x] = make_int4(0, 0, 0, 0);
+    }
+  };
 
   const int64_t T = int64_t(Hkv) * cum_nb[S];
   const int64_t U = int64_t(Hkv) * cum_np[S];
   const int64_t nunits = PB ? U : T;
   const int W = int(p.num_workers < nunits ? int64_t(p.num_workers) : nunits);
   const int w = blockIdx.x * kWarps + warp;
-  if (w >= W) return;
+  if (w >= W) {                              // no tiles for this warp
+    griddep_wait();
+    griddep_launch_dependents();
+    zero_empty();
+    return;
+  }
 
   auto locate = [&](int64_t t) -> Tile {
     Tile r;
@@ -297,6 +300,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     for (int bx = 0; bx < C::kNBox; ++bx)
       tma_load_2d(kdst + C::kTileBytes + bx * 2048, &tmv, bar, bx * C::kBoxElems, y, pol);
   };
+
+  // Up to here the kernel has read only lengths and block tables.  The cache, the queries,
+  // the outputs and the workspace are touched only after the preceding kernel on the stream
+  // (typically the KV write of this step) has finished.
+  griddep_wait();
+  griddep_launch_dependents();
+  zero_empty();
 
   Tile pc = locate(t_begin);                 // producer cursor, kStages tiles ahead
   for (int i = 0; i < min(n, kStages); ++i) {
@@ -561,31 +571,33 @@ __global__ void __launch_bounds__(kMergeWarps * 32) split_kv_merge_kernel(const 
   const int w0 = d.x, npieces = d.y;
   if (npieces <= 1) return;
   auto slot_of = [&](int k) -> int64_t { return k == 0 ? 2 * int64_t(w0) + d.z : 2 * int64_t(w0 + k); };
-  float M = -INFINITY;
-  for (int k = lane; k < npieces; k += 32) M = fmaxf(M, p.ml[slot_of(k) * G + hh].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // One pass with a running maximum; the loads of different pieces do not depend on each
+  // other, so an unrolled group of pieces is fetched together.
   constexpr int kVec = D / 32;
   float acc[kVec];
 #pragma unroll
   for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
-  float den = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 8
-    for (int k = 0; k < npieces; ++k) {
-      const int64_t sk = slot_of(k);
-      const float2 ml = p.ml[sk * G + hh];
-      const float wk = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-      den += wk * ml.y;
-      const float* src = p.po + (sk * G + hh) * D + lane * kVec;
-      if constexpr (kVec == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += wk * v.x; acc[1] += wk * v.y; acc[2] += wk * v.z; acc[3] += wk * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += wk * v.x; acc[1] += wk * v.y;
-      }
+  float M = -INFINITY, den = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < npieces; ++k) {
+    const int64_t sk = slot_of(k);
+    const float2 ml = p.ml[sk * G + hh];
+    const float* src = p.po + (sk * G + hh) * D + lane * kVec;
+    float v[kVec];
+    if constexpr (kVec == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      v[0] = t.x; v[1] = t.y;
     }
+    if (ml.x == -INFINITY) continue;                       // an empty piece contributes nothing
+    const float Mn = fmaxf(M, ml.x);
+    const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn);   // a = 0 while M = -inf
+    den = den * a + w * ml.y;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) acc[e] = acc[e] * a + w * v[e];
+    M = Mn;
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const int64_t obase = (int64_t(seg) * G + hh) * D + lane * kVec;   // out[s][h * G + hh][:]
