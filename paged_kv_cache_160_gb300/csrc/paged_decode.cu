@@ -15,9 +15,11 @@
 //     tile list (sequence-major, kv head, block) is cut into equal contiguous ranges, one
 //     per worker ("balanced" split), or into equal runs of whole partition_size-token
 //     partitions.  A worker's online softmax runs across consecutive partitions.
-//   * Each worker warp owns a ring of TMA stages: lane 0 issues 2-D tensor loads of the K
-//     and V tile (128-byte swizzled) straight from the physical block named by the block
-//     table, completing on an mbarrier; the warp waits, computes, and refills the stage.
+//   * Each worker warp owns a ring of TMA stages: lane 0 issues one tensor load for the K
+//     tile and one for the V tile (128-byte swizzled; a 256-byte row arrives as two swizzled
+//     halves) straight from the physical block named by the block table, completing on an
+//     mbarrier; the warp waits, computes, and refills the stage.  (TMA instruction issue, not
+//     bytes, limits small boxes, so each tile is a single box.)
 //   * All query heads of a kv head (group <= 8) are processed together on tensor cores:
 //     S^T[16 tok x 8 heads] = K[16 x D] * Q^T (m16n8k16, K as the A operand from ldmatrix),
 //     online softmax in registers (warp shuffles over the 16 tokens), P^T transposed with
@@ -48,7 +50,6 @@ struct Cfg {
   static constexpr int kElt = KV == KV_E4M3 ? 1 : 2;
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kNBox = kRowBytes / 128;       // 128-byte-wide TMA boxes per row
-  static constexpr int kBoxElems = 128 / kElt;
   static constexpr int kTileBytes = kBS * kRowBytes;  // one 16-row K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kKSteps = D / 16;
@@ -294,11 +295,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     mbar_arrive_expect_tx(bar, C::kStageBytes);
     const int y = int((int64_t(pb) * Hkv + c.h) * kBS);
     uint8_t* kdst = my_stages + st * C::kStageBytes;
-#pragma unroll
-    for (int bx = 0; bx < C::kNBox; ++bx) tma_load_2d(kdst + bx * 2048, &tmk, bar, bx * C::kBoxElems, y, pol);
-#pragma unroll
-    for (int bx = 0; bx < C::kNBox; ++bx)
-      tma_load_2d(kdst + C::kTileBytes + bx * 2048, &tmv, bar, bx * C::kBoxElems, y, pol);
+    if constexpr (C::kNBox == 2) {
+      // One 3-D box brings both 128-byte halves of the 16 rows: [half 0: 16 x 128 B][half 1].
+      tma_load_3d(kdst, &tmk, bar, 0, y, 0, pol);
+      tma_load_3d(kdst + C::kTileBytes, &tmv, bar, 0, y, 0, pol);
+    } else {
+      tma_load_2d(kdst, &tmk, bar, 0, y, pol);
+      tma_load_2d(kdst + C::kTileBytes, &tmv, bar, 0, y, pol);
+    }
   };
 
   // Up to here the kernel has read only lengths and block tables.  The cache, the queries,
@@ -738,16 +742,23 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
 
-  // Tensor maps: the pool as rows of head_dim elements, boxes of 16 rows x 128 bytes.
+  // Tensor maps: the pool as rows of head_dim elements; a box is one (block, kv head) tile of
+  // 16 rows.  Rows of 128 bytes are one 2-D box; rows of 256 bytes (2-byte, head_dim 128) are
+  // viewed as (64 elements, rows, 2 halves) so one 3-D box lands as two swizzled halves.
   CUtensorMap tk, tv;
   const bool fp8 = cache->kv_dtype == PKV_FP8_E4M3;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
   const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * kBS;
   const uint64_t row_bytes = uint64_t(D) * dtype_bytes(cache->kv_dtype);
-  const uint32_t box0 = fp8 ? 128 : 64;
-  if (!encode_tmap_2d(&tk, dt, k_cache, D, rows, row_bytes, box0, kBS, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tv, dt, v_cache, D, rows, row_bytes, box0, kBS, CU_TENSOR_MAP_SWIZZLE_128B))
-    return PKV_ERR_CUDA;
+  bool enc;
+  if (row_bytes == 256) {
+    enc = encode_tmap_3d(&tk, dt, k_cache, 64, rows, 2, 256, 128, 64, kBS, 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
+          encode_tmap_3d(&tv, dt, v_cache, 64, rows, 2, 256, 128, 64, kBS, 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    enc = encode_tmap_2d(&tk, dt, k_cache, D, rows, row_bytes, uint32_t(D), kBS, CU_TENSOR_MAP_SWIZZLE_128B) &&
+          encode_tmap_2d(&tv, dt, v_cache, D, rows, row_bytes, uint32_t(D), kBS, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!enc) return PKV_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeParams prm;

@@ -7,19 +7,27 @@
 // (§2.2–§2.3) — the same paged cache the decode kernel reads.
 //
 // GB300 design (one CTA per 128 query rows of one query head, 1 CTA per SM):
-//   warp 0, one thread : TMA producer — Q once (128 rows x 128 dims), then per 128-key tile
+//   warp 0             : TMA producer — Q once (128 rows x 128 dims), then per 128-key tile
 //                        the 8 physical blocks of K and of V (16-row boxes gathered by block
-//                        id), double buffered.
+//                        id; the block table is read 32 entries at a time, lane-parallel, one
+//                        window ahead; one 3-D TMA box per block brings both 128-byte halves
+//                        of its 16 rows); K (3 stages) runs ahead of V (2 stages), each stage
+//                        refilled as soon as its MMA is done.
 //   warp 1             : owns 512 TMEM columns; one thread issues tcgen05.mma —
-//                        S_j = Q K_j^T (M = N = 128, K = 128, both operands K-major in smem)
-//                        into one of two TMEM S buffers, and O += P_{j-1} V_{j-1} (P K-major,
-//                        V MN-major) into the TMEM O accumulator, so S_j overlaps softmax_{j-1}.
-//   warps 4..7         : softmax, one query row per thread (TMEM lane = row): causal mask,
-//                        online softmax in base 2, P (bf16/f16) written to shared memory in
-//                        the 128-byte-swizzled K-major layout the MMA reads.  The running max
-//                        used for the exponents is only moved (and O rescaled in TMEM) when
-//                        the row max grows by more than 2^8, so most tiles skip the rescale;
-//                        the final division by the same-base sum keeps the result exact.
+//                        S_j = Q K_j^T (M = 128, two N = 64 halves, K = 128, both operands
+//                        K-major in smem) into one of two TMEM S buffers, and O += P_{j-1} V_{j-1} into the TMEM
+//                        O accumulator, with P read from TMEM (it overwrites S_{j-1} in place)
+//                        and V from shared memory as an MN-major operand.  S_j overlaps
+//                        softmax_{j-1}, and the softmax never waits for a PV product unless it
+//                        must rescale O.
+//   warps 2..9         : softmax, two warpgroups; each thread owns one query row (TMEM lane)
+//                        and one half of its 128 columns, the halves swap only the tile's row
+//                        max.  Causal mask on diagonal tiles, online softmax in base 2
+//                        (2^(s*scale*log2e - m): one FFMA and one ex2 per score), P (bf16/f16)
+//                        stored to TMEM over the tile's S.  The running max used for the exponents is only moved (and
+//                        O rescaled in TMEM) when the row max grows by more than 2^8, so most
+//                        tiles skip the rescale; the final division by the same-base sum keeps
+//                        the result exact.
 // Every wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA drains and exits.
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -30,11 +38,16 @@ namespace {
 constexpr int kBS = 16;
 constexpr int kD = 128;
 constexpr int kTile = 128;                    // query rows per CTA and keys per iteration
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O (128 columns each) rounded up
 constexpr int kHalfBytes = kTile * 128;       // [128 rows][64 elements] of 2 bytes = 16 KB
 constexpr int kTileBytes = 2 * kHalfBytes;    // one 128 x 128 operand = 32 KB
-constexpr int kSmemBytes = 1024 + 6 * kTileBytes;   // Q, K[2], V[2], P
+// K and V tiles hold 8 blocks of 4 KB: block b at 4 KB * b = [dims 0..63: 16 rows x 128 B]
+// [dims 64..127: 16 rows x 128 B], each half 128-byte swizzled (one TMA box per block).
+constexpr int kBlockBytes = kBS * kD * 2;
+constexpr int kKStages = 3;                   // K tiles in flight (released when their S product is done)
+constexpr int kVStages = 2;                   // V tiles in flight (released when their PV product is done)
+constexpr int kSmemBytes = 1024 + (1 + kKStages + kVStages) * kTileBytes;   // Q, K stages, V stages
 constexpr float kRescaleThreshold = 8.f;      // log2 units
 
 struct PrefillParams {
@@ -60,8 +73,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_kv_full[2], bar_kv_empty[2], bar_s_full[2], bar_p_full, bar_pv_done;
+  __shared__ __align__(8) uint64_t bar_q, bar_k_full[kKStages], bar_k_empty[kKStages], bar_v_full[kVStages],
+      bar_v_empty[kVStages], bar_s_full[2], bar_p_full[2], bar_pv_done;
   __shared__ uint32_t tmem_base_sh;
+  __shared__ float row_xchg[2][2][kTile];                    // [use parity][half][row]: values the softmax halves swap
+  __shared__ __align__(8) uint64_t bar_xchg[2];              // 256 arrivals: both halves have written
 
   const int qt = blockIdx.x, hq = blockIdx.y, c = blockIdx.z;
   const int q0 = p.cu_q_lens[c];
@@ -84,9 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTileBytes;                           // two stages
-  uint8_t* sV = smem + 3 * kTileBytes;                       // two stages
-  uint8_t* sP = smem + 5 * kTileBytes;
+  uint8_t* sK = smem + kTileBytes;                           // kKStages stages
+  uint8_t* sV = smem + (1 + kKStages) * kTileBytes;          // kVStages stages
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -94,12 +109,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
     mbar_init(&bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_kv_full[i], 1);
-      mbar_init(&bar_kv_empty[i], 1);
-      mbar_init(&bar_s_full[i], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bar_k_full[i], 1);
+      mbar_init(&bar_k_empty[i], 1);
     }
-    mbar_init(&bar_p_full, 128);
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bar_v_full[i], 1);
+      mbar_init(&bar_v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_p_full[i], 256);
+    }
+    mbar_init(&bar_xchg[0], 256);
+    mbar_init(&bar_xchg[1], 256);
     mbar_init(&bar_pv_done, 1);
     fence_mbar_init();
   }
@@ -113,123 +136,233 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0) {
+    // ---------------- TMA producer (the whole warp; lane 0 issues) ----------------
     const uint64_t pol_q = l2_policy_evict_first();
     const uint64_t pol_kv = l2_policy_evict_last();          // re-read by the other query heads
-    mbar_arrive_expect_tx(&bar_q, kTileBytes);
-    tma_load_3d(sQ, &tmq, &bar_q, 0, hq, q0 + r0, pol_q);
-    tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq, q0 + r0, pol_q);
-    int issued = 0;
-    for (int j = 0; j < nt; ++j) {
-      const int st = j & 1;
-      if (j >= 2 && !mbar_wait(&bar_kv_empty[st], uint32_t((j - 2) >> 1) & 1u)) {
-        set_error(p.err, PKV_DEVERR_TIMEOUT);
-        break;
-      }
-      mbar_arrive_expect_tx(&bar_kv_full[st], 2 * kTileBytes);
-      for (int b = 0; b < kTile / kBS; ++b) {
-        const int lb = j * (kTile / kBS) + b;
-        int pb = 0;                                          // blocks past the sequence: any valid
-        if (lb < nb) {                                       // block; their rows are masked / zeroed
-          pb = table[lb];
-          if (pb < 0 || pb >= p.num_blocks) {
-            set_error(p.err, PKV_DEVERR_BLOCK_ID);
-            pb = 0;
-          }
-        }
-        const int y = (pb * p.num_kv_heads + h) * kBS;
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_load_2d(sK + st * kTileBytes + hf * kHalfBytes + b * 2048, &tmk, &bar_kv_full[st], hf * 64, y, pol_kv);
-          tma_load_2d(sV + st * kTileBytes + hf * kHalfBytes + b * 2048, &tmv, &bar_kv_full[st], hf * 64, y, pol_kv);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, kTileBytes);
+      tma_load_3d(sQ, &tmq, &bar_q, 0, hq, q0 + r0, pol_q);
+      tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq, q0 + r0, pol_q);
+    }
+    // Pool rows of the sequence's logical blocks, 32 per window (4 tiles): lane i holds block
+    // 32 * w + i.  Blocks past the sequence map to block 0 (their rows are masked / zeroed).
+    auto load_window = [&](int w) -> int {
+      const int lb = 32 * w + lane;
+      int pb = 0;
+      if (lb < nb) {
+        pb = table[lb];
+        if (pb < 0 || pb >= p.num_blocks) {
+          set_error(p.err, PKV_DEVERR_BLOCK_ID);
+          pb = 0;
         }
       }
-      issued = j + 1;
+      return (pb * p.num_kv_heads + h) * kBS;
+    };
+    struct Window {
+      int cur, nxt, w;
+    };
+    // The window holding tile j (one ahead is always loaded, so the loads overlap the TMAs).
+    auto seek = [&](Window& win, int j) {
+      while (j / 4 > win.w) {
+        win.cur = win.nxt;
+        ++win.w;
+        win.nxt = load_window(win.w + 1);
+      }
+    };
+    Window wk{load_window(0), load_window(1), 0};
+    Window wv = wk;
+    auto issue_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, Window& win, int j) {
+      seek(win, j);
+      int rows[kTile / kBS];
+#pragma unroll
+      for (int b = 0; b < kTile / kBS; ++b) rows[b] = __shfl_sync(0xffffffffu, win.cur, (8 * j) % 32 + b);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, kTileBytes);
+#pragma unroll
+        for (int b = 0; b < kTile / kBS; ++b) tma_load_3d(dst + b * kBlockBytes, map, bar, 0, rows[b], 0, pol_kv);
+      }
+    };
+    // K runs ahead of V; each is issued as soon as its stage has been released.  Lane 0
+    // polls the barriers and broadcasts, so the warp stays converged.
+    auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
+      uint32_t r = 0;
+      if (lane == 0) r = mbar_try_wait(bar, parity) ? 1u : 0u;
+      return __shfl_sync(0xffffffffu, r, 0) != 0;
+    };
+    int kj = 0, vj = 0;
+    uint64_t t0 = 0;
+    bool ok = true;
+    while (ok && (kj < nt || vj < nt)) {
+      bool progress = false;
+      if (kj < nt && (kj < kKStages || ready(&bar_k_empty[kj % kKStages], uint32_t((kj - kKStages) / kKStages) & 1u))) {
+        issue_tile(&tmk, sK + (kj % kKStages) * kTileBytes, &bar_k_full[kj % kKStages], wk, kj);
+        ++kj;
+        progress = true;
+      }
+      if (vj < kj && (vj < kVStages || ready(&bar_v_empty[vj % kVStages], uint32_t((vj - kVStages) / kVStages) & 1u))) {
+        issue_tile(&tmv, sV + (vj % kVStages) * kTileBytes, &bar_v_full[vj % kVStages], wv, vj);
+        ++vj;
+        progress = true;
+      }
+      // Lane 0 keeps the clock, so every lane takes the same decision.  Idle polls back off
+      // so they do not take issue slots from the softmax warps on the same SM sub-partition.
+      if (!progress) __nanosleep(100);
+      uint32_t give_up = 0;
+      if (lane == 0) {
+        if (progress) {
+          t0 = 0;
+        } else if (t0 == 0) {
+          t0 = global_timer_ns();
+        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+          set_error(p.err, PKV_DEVERR_TIMEOUT);
+          give_up = 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
     }
     // Drain: the last load of each stage must have landed before the CTA may exit.
-    for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) (void)mbar_wait(&bar_kv_full[j & 1], uint32_t(j >> 1) & 1u);
+    if (lane == 0) {
+      for (int j = kj - kKStages < 0 ? 0 : kj - kKStages; j < kj; ++j)
+        (void)mbar_wait(&bar_k_full[j % kKStages], uint32_t(j / kKStages) & 1u);
+      for (int j = vj - kVStages < 0 ? 0 : vj - kVStages; j < vj; ++j)
+        (void)mbar_wait(&bar_v_full[j % kVStages], uint32_t(j / kVStages) & 1u);
+    }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc_s = umma_idesc_f16(kBF16, 128, 128, false, false);
+    // S_j needs K_j and a free S buffer (PV_{j-2}, which reads P_{j-2} from that buffer,
+    // issued: tcgen05 ops of one thread execute in order); PV_j needs P_j and V_j.  Whichever
+    // is ready is issued first.
+    const uint32_t idesc_s = umma_idesc_f16(kBF16, 128, 64, false, false);
     const uint32_t idesc_o = umma_idesc_f16(kBF16, 128, 128, false, true);
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
     bool ok = mbar_wait(&bar_q, 0);
-    for (int j = 0; ok && j <= nt; ++j) {
-      if (j < nt) {
-        const int st = j & 1;
-        if (!(ok = mbar_wait(&bar_kv_full[st], uint32_t(j >> 1) & 1u))) break;
+    int js = 0, jp = 0;
+    uint64_t t0 = 0;
+    while (ok && jp < nt) {
+      bool progress = false;
+      if (js < nt && js - jp < 2 && mbar_try_wait(&bar_k_full[js % kKStages], uint32_t(js / kKStages) & 1u)) {
         tc_fence_after();
-        const uint32_t tS = (j & 1) ? tS1 : tS0;
+        const int st = js % kKStages;
+        const uint32_t tS = (js & 1) ? tS1 : tS0;
+        // S columns 0..63 hold keys 16b + i (i < 8) of blocks b = 0..7, columns 64..127 keys
+        // 16b + 8 + i: in each set the 8-row groups of K sit 4 KB apart.
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_f16(tS, umma_sdesc_sw128(aQ + koff, 16, 1024), umma_sdesc_sw128(aK + st * kTileBytes + koff, 16, 1024),
-                   idesc_s, kk > 0);
+          const uint32_t qoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * (kBlockBytes / 2) + (kk & 3) * 32;
+          const uint64_t qd = umma_sdesc_sw128(aQ + qoff, 16, 1024);
+          umma_f16(tS, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff, 16, kBlockBytes), idesc_s, kk > 0);
+          umma_f16(tS + 64, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff + 1024, 16, kBlockBytes), idesc_s, kk > 0);
         }
-        umma_commit(&bar_s_full[j & 1]);
+        umma_commit(&bar_s_full[js & 1]);
+        umma_commit(&bar_k_empty[st]);
+        ++js;
+        progress = true;
       }
-      if (j >= 1) {
-        const int jj = j - 1, st = jj & 1;
-        if (!(ok = mbar_wait(&bar_p_full, uint32_t(jj) & 1u))) break;
+      if (jp < js && mbar_try_wait(&bar_p_full[jp & 1], uint32_t(jp >> 1) & 1u) &&
+          mbar_try_wait(&bar_v_full[jp % kVStages], uint32_t(jp / kVStages) & 1u)) {
         tc_fence_after();
+        const int st = jp % kVStages;
+        // P_jp sits in the first 64 columns of its S buffer, two 16-bit values per column.
+        const uint32_t tP = (jp & 1) ? tS1 : tS0;
+        // k-step kk covers P columns 16kk .. 16kk + 15: blocks 2kk', 2kk' + 1 (kk' = kk % 4),
+        // rows 0..7 for kk < 4 and rows 8..15 after.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_f16(tO, umma_sdesc_sw128(aP + poff, 16, 1024),
-                   umma_sdesc_sw128(aV + st * kTileBytes + kk * 2048, kHalfBytes, 1024), idesc_o, jj > 0 || kk > 0);
+          const uint32_t voff = (kk & 3) * 2 * kBlockBytes + (kk >> 2) * 1024;
+          umma_f16_ts(tO, tP + 8 * kk, umma_sdesc_sw128(aV + st * kTileBytes + voff, kBlockBytes / 2, kBlockBytes),
+                      idesc_o, jp > 0 || kk > 0);
         }
         umma_commit(&bar_pv_done);
-        umma_commit(&bar_kv_empty[st]);
+        umma_commit(&bar_v_empty[st]);
+        ++jp;
+        progress = true;
+      }
+      if (progress) {
+        t0 = 0;
+      } else {
+        __nanosleep(50);
+        if (t0 == 0) {
+          t0 = global_timer_ns();
+        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+          ok = false;
+        }
       }
     }
     if (!ok) set_error(p.err, PKV_DEVERR_TIMEOUT);
-  } else if (warp >= 4) {
-    // ---------------- softmax warpgroup: one query row per thread ----------------
-    const int r = threadIdx.x - 128;                         // TMEM lane == row of the tile
+  } else if (warp >= 2) {
+    // ---------------- softmax: two warpgroups, one query row per thread in each ----------
+    // Warp w reaches TMEM lanes 32 * (w % 4) .. + 31, so warps 2..5 and 6..9 each cover all
+    // 128 rows; warpgroup `half` owns columns 64 * half .. + 63 of S, O and P.
+    const int half = (warp - 2) >> 2;
+    const int r = 32 * (warp & 3) + lane;                    // TMEM lane == row of the tile
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+    const uint32_t col0 = 64 * half;
     const int qrow = r0 + r;
     const int pos = start + qrow;                            // absolute position of this query
-    const uint32_t aP = smem_u32(sP);
-    float m = -INFINITY, l = 0.f;
+    const float sl = p.scale_log2;                           // > 0, so max(s) * sl = max(s * sl)
+    // Swap one float per row with the other half through shared memory; the k-th swap uses
+    // buffer and barrier k % 2 (bounded wait; the barrier's arrive/wait order the accesses).
+    int n_swaps = 0;
+    auto swap_halves = [&](float mine, float& theirs) -> bool {
+      const int b = n_swaps & 1;
+      row_xchg[b][half][r] = mine;
+      mbar_arrive(&bar_xchg[b]);
+      const bool done = mbar_wait(&bar_xchg[b], uint32_t(n_swaps >> 1) & 1u);
+      theirs = row_xchg[b][half ^ 1][r];
+      ++n_swaps;
+      return done;
+    };
+    float m = -INFINITY, l = 0.f;                            // m in scaled log2 units
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       if (!(ok = mbar_wait(&bar_s_full[j & 1], uint32_t(j >> 1) & 1u))) break;
       __syncwarp();
       tc_fence_after();
-      float s[kTile];
-#pragma unroll
-      for (int cc = 0; cc < kTile / 32; ++cc) {
+      float s[64];
+      {
         float v[32];
-        tmem_ld32(((j & 1) ? tS1 : tS0) + lane_off + 32 * cc, v);
+        const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off + col0;
+        tmem_ld32(tS, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * cc + i] = v[i];
+        for (int i = 0; i < 32; ++i) s[i] = v[i];
+        tmem_ld32(tS + 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
       }
       tmem_wait_ld();
-      const int kb = j * kTile;
-      const int lim = min(pos + 1, ctx) - kb;                // keys kb + i valid for i < lim
-      float mt = -INFINITY;
+      // Column i of this half holds key kb + 16 * (i / 8) + 8 * half + i % 8 (see the MMA).
+      const int lim = min(pos + 1, ctx) - (j * kTile + 8 * half);   // valid iff 16*(i/8) + i%8 < lim
+      float mraw = -INFINITY;
+      if (lim >= kTile) {
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) {
-        s[i] = i < lim ? s[i] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[i]);
+        for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          s[i] = 16 * (i >> 3) + (i & 7) < lim ? s[i] : -INFINITY;
+          mraw = fmaxf(mraw, s[i]);
+        }
       }
-      // P buffer free and O up to date once the previous PV product is done.
-      if (j >= 1) {
-        if (!(ok = mbar_wait(&bar_pv_done, uint32_t(j - 1) & 1u))) break;
-        tc_fence_after();
-      }
+      float other;
+      if (!(ok = swap_halves(mraw, other))) break;
+      const float mt = fmaxf(mraw, other) * sl;              // row max of the tile
       const bool grow = mt > m + kRescaleThreshold;          // also true for the first tile
-      __syncwarp();
       if (__any_sync(0xffffffffu, grow && j >= 1)) {
+        // O must be up to date (the previous PV product done) before it is rescaled.
+        if (!(ok = mbar_wait(&bar_pv_done, uint32_t(j - 1) & 1u))) break;
+        __syncwarp();
+        tc_fence_after();
         const float alpha = (grow && m != -INFINITY) ? fast_exp2(m - mt) : 1.f;
 #pragma unroll
-        for (int cc = 0; cc < kD / 32; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float v[32];
-          tmem_ld32(tO + lane_off + 32 * cc, v);
+          tmem_ld32(tO + lane_off + col0 + 32 * cc, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tmem_st32(tO + lane_off + 32 * cc, v);
+          tmem_st32(tO + lane_off + col0 + 32 * cc, v);
         }
         tmem_wait_st();
         if (grow) l *= alpha;
@@ -237,50 +370,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (grow) m = mt;
       // The last key tile may reach past the sequence: zero those V rows so that 0 * garbage
       // cannot turn into NaN inside the PV product.
+      const int kb = j * kTile;
       if (kb + kTile > ctx) {
-        if (!(ok = mbar_wait(&bar_kv_full[j & 1], uint32_t(j >> 1) & 1u))) break;
+        if (!(ok = mbar_wait(&bar_v_full[j % kVStages], uint32_t(j / kVStages) & 1u))) break;
         if (kb + r >= ctx) {
-          const uint32_t vrow = smem_u32(sV + (j & 1) * kTileBytes) + r * 128;
+          const uint32_t vrow = smem_u32(sV + (j % kVStages) * kTileBytes) + (r / kBS) * kBlockBytes +
+                                half * (kBlockBytes / 2) + (r % kBS) * 128;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) sts128(vrow + hf * kHalfBytes + cc * 16, 0u, 0u, 0u, 0u);
+          for (int cc = 0; cc < 8; ++cc) sts128(vrow + cc * 16, 0u, 0u, 0u, 0u);
         }
       }
-      // P = 2^(s - m), written as the A operand (K-major, 128-byte swizzle).
+      // P = 2^(s * sl - m) as 16-bit pairs, written over this tile's S in TMEM: keys
+      // 64 * half .. + 63 go to columns 32 * half .. + 31 (the S values are in registers).
       float lsum = 0.f;
+      uint32_t w[32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = fast_exp2(s[64 * hf + 8 * cc + 2 * e] - m);
-            const float b = fast_exp2(s[64 * hf + 8 * cc + 2 * e + 1] - m);
-            lsum += a + b;
-            w[e] = pack_out<kBF16>(a, b);
-          }
-          sts128(aP + hf * kHalfBytes + r * 128 + ((cc ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
-        }
+      for (int e = 0; e < 32; ++e) {
+        const float a = fast_exp2(fmaf(s[2 * e], sl, -m));
+        const float b = fast_exp2(fmaf(s[2 * e + 1], sl, -m));
+        lsum += a + b;
+        w[e] = pack_out<kBF16>(a, b);
       }
+      tmem_st32u(((j & 1) ? tS1 : tS0) + lane_off + 32 * half, w);
+      tmem_wait_st();
       l += lsum;
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();                              // the zeroed V rows, if any
       tc_fence_before();
-      mbar_arrive(&bar_p_full);
+      mbar_arrive(&bar_p_full[j & 1]);
     }
     if (ok) ok = mbar_wait(&bar_pv_done, uint32_t(nt - 1) & 1u);
+    // Row sum = the two halves' partial sums (both used the same m).
+    if (ok) {
+      float other;
+      ok = swap_halves(l, other);
+      l += other;
+    }
     __syncwarp();
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool live = qrow < qlen;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                            ((int64_t(q0) + qrow) * p.num_heads + hq) * (kD * 2));
+                                            ((int64_t(q0) + qrow) * p.num_heads + hq) * (kD * 2) + col0 * 2);
 #pragma unroll
-      for (int cc = 0; cc < kD / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         float v[32];
-        tmem_ld32(tO + lane_off + 32 * cc, v);
+        tmem_ld32(tO + lane_off + col0 + 32 * cc, v);
         tmem_wait_ld();
         if (live) {
 #pragma unroll
@@ -291,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           pack_out<kBF16>(v[8 * q4 + 6] * inv, v[8 * q4 + 7] * inv));
         }
       }
-    } else if (threadIdx.x == 128) {
+    } else if (r == 0 && half == 0) {
       set_error(p.err, PKV_DEVERR_TIMEOUT);
     }
     tc_fence_before();
@@ -328,6 +463,7 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   if (cache->kv_dtype != q_dtype || cache->head_dim != kD || cache->block_size != kBS) return PKV_ERR_UNSUPPORTED;
   if (num_chunks > 65535 || num_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!(scale > 0.f)) return PKV_ERR_INVALID_ARG;          // the softmax takes max(s) * scale
   if (int64_t(cache->num_blocks) * cache->num_kv_heads * kBS >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
@@ -336,9 +472,10 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * kBS;
   if (!encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, q, kD, uint64_t(num_heads), uint64_t(total_q), kD * 2,
                       uint64_t(num_heads) * kD * 2, 64, 1, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, k_cache, kD, rows, kD * 2, 64, kBS,
+      // K / V as (64 dims, rows, 2 halves): one box = a block's 16 rows of both halves
+      !encode_tmap_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, k_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 2,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, v_cache, kD, rows, kD * 2, 64, kBS,
+      !encode_tmap_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, v_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 2,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return PKV_ERR_CUDA;
 
