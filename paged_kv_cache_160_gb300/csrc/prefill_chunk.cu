@@ -11,23 +11,23 @@
 //                        the 8 physical blocks of K and of V (16-row boxes gathered by block
 //                        id; the block table is read 32 entries at a time, lane-parallel, one
 //                        window ahead; one 3-D TMA box per block brings both 128-byte halves
-//                        of its 16 rows); K (3 stages) runs ahead of V (2 stages), each stage
+//                        of its 16 rows); K and V (3 stages each) run ahead, each stage
 //                        refilled as soon as its MMA is done.
 //   warp 1             : owns 512 TMEM columns; one thread issues tcgen05.mma —
 //                        S_j = Q K_j^T (M = 128, two N = 64 halves, K = 128, both operands
-//                        K-major in smem) into one of two TMEM S buffers, and O += P_{j-1} V_{j-1} into the TMEM
-//                        O accumulator, with P read from TMEM (it overwrites S_{j-1} in place)
-//                        and V from shared memory as an MN-major operand.  S_j overlaps
-//                        softmax_{j-1}, and the softmax never waits for a PV product unless it
-//                        must rescale O.
+//                        K-major in smem) into one of three TMEM S buffers, and
+//                        O += P_j V_j into the TMEM O accumulator, with P read from TMEM (it
+//                        overwrites S_j in place) and V from shared memory as an MN-major
+//                        operand.  S of later tiles overlaps the softmax of earlier ones, and
+//                        the softmax never waits for a PV product unless it must rescale O.
 //   warps 2..9         : softmax, two warpgroups; each thread owns one query row (TMEM lane)
 //                        and one half of its 128 columns, the halves swap only the tile's row
 //                        max.  Causal mask on diagonal tiles, online softmax in base 2
 //                        (2^(s*scale*log2e - m): one FFMA and one ex2 per score), P (bf16/f16)
-//                        stored to TMEM over the tile's S.  The running max used for the exponents is only moved (and
-//                        O rescaled in TMEM) when the row max grows by more than 2^8, so most
-//                        tiles skip the rescale; the final division by the same-base sum keeps
-//                        the result exact.
+//                        stored to TMEM over the tile's S.  The running max used for the
+//                        exponents is only moved (and O rescaled in TMEM) when the row max
+//                        grows by more than 2^8, so most tiles skip the rescale; the final
+//                        division by the same-base sum keeps the result exact.
 // Every wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA drains and exits.
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -39,15 +39,19 @@ constexpr int kBS = 16;
 constexpr int kD = 128;
 constexpr int kTile = 128;                    // query rows per CTA and keys per iteration
 constexpr int kThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
-constexpr uint32_t kTmemCols = 512;           // S0 | S1 | O (128 columns each) rounded up
+constexpr uint32_t kTmemCols = 512;           // S0 | S1 | S2 | O, 128 columns each
 constexpr int kHalfBytes = kTile * 128;       // [128 rows][64 elements] of 2 bytes = 16 KB
 constexpr int kTileBytes = 2 * kHalfBytes;    // one 128 x 128 operand = 32 KB
 // K and V tiles hold 8 blocks of 4 KB: block b at 4 KB * b = [dims 0..63: 16 rows x 128 B]
 // [dims 64..127: 16 rows x 128 B], each half 128-byte swizzled (one TMA box per block).
 constexpr int kBlockBytes = kBS * kD * 2;
 constexpr int kKStages = 3;                   // K tiles in flight (released when their S product is done)
-constexpr int kVStages = 2;                   // V tiles in flight (released when their PV product is done)
-constexpr int kSmemBytes = 1024 + (1 + kKStages + kVStages) * kTileBytes;   // Q, K stages, V stages
+constexpr int kVStages = 3;                   // V tiles in flight (released when their PV product is done)
+constexpr int kSBufs = 3;                     // TMEM S/P buffers (128 columns each; O takes the 4th)
+// Q, K stages, V stages: 224 KB, which with the static barriers fills the 227 KB a CTA may
+// use, so the dynamic region carries no alignment slack; the kernel checks that it starts on
+// a 1 KB boundary (required by the 128-byte swizzle) and reports an error otherwise.
+constexpr int kSmemBytes = (1 + kKStages + kVStages) * kTileBytes;
 constexpr float kRescaleThreshold = 8.f;      // log2 units
 
 struct PrefillParams {
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_k_full[kKStages], bar_k_empty[kKStages], bar_v_full[kVStages],
-      bar_v_empty[kVStages], bar_s_full[2], bar_p_full[2], bar_pv_done;
+      bar_v_empty[kVStages], bar_s_full[kSBufs], bar_p_full[kSBufs], bar_pv_done;
   __shared__ uint32_t tmem_base_sh;
   __shared__ float row_xchg[2][2][kTile];                    // [use parity][half][row]: values the softmax halves swap
   __shared__ __align__(8) uint64_t bar_xchg[2];              // 256 arrivals: both halves have written
@@ -98,7 +102,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = (ctx + kBS - 1) / kBS;
   const int32_t* table = p.block_tables + int64_t(c) * p.max_blocks;
 
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {                              // see kSmemBytes
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
+    return;
+  }
   uint8_t* sQ = smem;
   uint8_t* sK = smem + kTileBytes;                           // kKStages stages
   uint8_t* sV = smem + (1 + kKStages) * kTileBytes;          // kVStages stages
@@ -117,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_v_full[i], 1);
       mbar_init(&bar_v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bar_s_full[i], 1);
       mbar_init(&bar_p_full[i], 256);
     }
@@ -134,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+  const uint32_t tO = tmem + 128 * kSBufs;
+  auto tS = [&](int j) -> uint32_t { return tmem + 128 * uint32_t(j % kSBufs); };   // S_j, then P_j
 
   if (warp == 0) {
     // ---------------- TMA producer (the whole warp; lane 0 issues) ----------------
@@ -172,16 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     Window wk{load_window(0), load_window(1), 0};
     Window wv = wk;
+    // The 8 lanes that hold the tile's block rows issue one box each, in the same instruction.
     auto issue_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, Window& win, int j) {
       seek(win, j);
-      int rows[kTile / kBS];
-#pragma unroll
-      for (int b = 0; b < kTile / kBS; ++b) rows[b] = __shfl_sync(0xffffffffu, win.cur, (8 * j) % 32 + b);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, kTileBytes);
-#pragma unroll
-        for (int b = 0; b < kTile / kBS; ++b) tma_load_3d(dst + b * kBlockBytes, map, bar, 0, rows[b], 0, pol_kv);
-      }
+      const int first = (8 * j) % 32;
+      if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
+      __syncwarp();
+      if (lane >= first && lane < first + kTile / kBS)
+        tma_load_3d(dst + (lane - first) * kBlockBytes, map, bar, 0, win.cur, 0, pol_kv);
     };
     // K runs ahead of V; each is issued as soon as its stage has been released.  Lane 0
     // polls the barriers and broadcasts, so the warp stays converged.
@@ -241,10 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t t0 = 0;
     while (ok && jp < nt) {
       bool progress = false;
-      if (js < nt && js - jp < 2 && mbar_try_wait(&bar_k_full[js % kKStages], uint32_t(js / kKStages) & 1u)) {
+      if (js < nt && js - jp < kSBufs && mbar_try_wait(&bar_k_full[js % kKStages], uint32_t(js / kKStages) & 1u)) {
         tc_fence_after();
         const int st = js % kKStages;
-        const uint32_t tS = (js & 1) ? tS1 : tS0;
+        const uint32_t tSj = tS(js);
         // S columns 0..63 hold keys 16b + i (i < 8) of blocks b = 0..7, columns 64..127 keys
         // 16b + 8 + i: in each set the 8-row groups of K sit 4 KB apart.
 #pragma unroll
@@ -252,20 +259,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * (kBlockBytes / 2) + (kk & 3) * 32;
           const uint64_t qd = umma_sdesc_sw128(aQ + qoff, 16, 1024);
-          umma_f16(tS, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff, 16, kBlockBytes), idesc_s, kk > 0);
-          umma_f16(tS + 64, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff + 1024, 16, kBlockBytes), idesc_s, kk > 0);
+          umma_f16(tSj, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff, 16, kBlockBytes), idesc_s, kk > 0);
+          umma_f16(tSj + 64, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff + 1024, 16, kBlockBytes), idesc_s, kk > 0);
         }
-        umma_commit(&bar_s_full[js & 1]);
+        umma_commit(&bar_s_full[js % kSBufs]);
         umma_commit(&bar_k_empty[st]);
         ++js;
         progress = true;
       }
-      if (jp < js && mbar_try_wait(&bar_p_full[jp & 1], uint32_t(jp >> 1) & 1u) &&
+      if (jp < js && mbar_try_wait(&bar_p_full[jp % kSBufs], uint32_t(jp / kSBufs) & 1u) &&
           mbar_try_wait(&bar_v_full[jp % kVStages], uint32_t(jp / kVStages) & 1u)) {
         tc_fence_after();
         const int st = jp % kVStages;
         // P_jp sits in the first 64 columns of its S buffer, two 16-bit values per column.
-        const uint32_t tP = (jp & 1) ? tS1 : tS0;
+        const uint32_t tP = tS(jp);
         // k-step kk covers P columns 16kk .. 16kk + 15: blocks 2kk', 2kk' + 1 (kk' = kk % 4),
         // rows 0..7 for kk < 4 and rows 8..15 after.
 #pragma unroll
@@ -317,17 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;                            // m in scaled log2 units
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      if (!(ok = mbar_wait(&bar_s_full[j & 1], uint32_t(j >> 1) & 1u))) break;
+      if (!(ok = mbar_wait(&bar_s_full[j % kSBufs], uint32_t(j / kSBufs) & 1u))) break;
       __syncwarp();
       tc_fence_after();
       float s[64];
       {
         float v[32];
-        const uint32_t tS = ((j & 1) ? tS1 : tS0) + lane_off + col0;
-        tmem_ld32(tS, v);
+        const uint32_t tSj = tS(j) + lane_off + col0;
+        tmem_ld32(tSj, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[i] = v[i];
-        tmem_ld32(tS + 32, v);
+        tmem_ld32(tSj + 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
       }
@@ -391,12 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         lsum += a + b;
         w[e] = pack_out<kBF16>(a, b);
       }
-      tmem_st32u(((j & 1) ? tS1 : tS0) + lane_off + 32 * half, w);
+      tmem_st32u(tS(j) + lane_off + 32 * half, w);
       tmem_wait_st();
       l += lsum;
       fence_proxy_async_smem();                              // the zeroed V rows, if any
       tc_fence_before();
-      mbar_arrive(&bar_p_full[j & 1]);
+      mbar_arrive(&bar_p_full[j % kSBufs]);
     }
     if (ok) ok = mbar_wait(&bar_pv_done, uint32_t(nt - 1) & 1u);
     // Row sum = the two halves' partial sums (both used the same m).
