@@ -98,6 +98,9 @@ PKV_API int pkv_version(void);       /* (major << 16) | minor */
  * in_dtype == kv_dtype copies bytes.  in_dtype f16/bf16 into an e4m3 cache quantises
  * x / scale[h] (fp32 divide) to e4m3, round-to-nearest-even, saturating at ±448.
  * Slots that repeat within one call: one of the writers wins (unspecified which).
+ * Launch order (kv_write and copy_blocks alike): launched as a programmatic dependent of
+ * the previous kernel on `stream`; the kernel touches no memory before that kernel has
+ * completed, so stream order holds as for a plain launch.
  */
 PKV_API pkv_status pkv_kv_write(const void* k_new, const void* v_new, pkv_dtype in_dtype, int num_tokens,
                         const int64_t* slot_mapping, void* k_cache, void* v_cache,

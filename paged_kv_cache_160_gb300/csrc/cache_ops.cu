@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kThreads) kv_write_copy_kernel(const uint4* __
                                                                  int num_kv_heads, int chunks, int block_size,
                                                                  int64_t num_slots, unsigned* err) {
   griddep_launch_dependents();   // a following decode may start its length-only prologue
+  griddep_wait();                // the previous kernel (which may read this cache) is done
   const int64_t total = int64_t(num_tokens) * num_kv_heads * chunks;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     const int c = int(i % chunks);
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kThreads) kv_write_quant_kernel(
     const float* __restrict__ v_scale, int num_tokens, int num_kv_heads, int chunks, int block_size,
     int64_t num_slots, unsigned* err) {
   griddep_launch_dependents();
+  griddep_wait();
   const int64_t total = int64_t(num_tokens) * num_kv_heads * chunks;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     const int c = int(i % chunks);
@@ -103,6 +105,8 @@ __global__ void __launch_bounds__(kThreads) copy_blocks_kernel(uint4* __restrict
                                                                uint4* __restrict__ v_cache,
                                                                const int32_t* __restrict__ pairs, int num_pairs,
                                                                int num_blocks, int64_t chunks, unsigned* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int pair = blockIdx.x;
   const int32_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
   // A pair is applied only when both ids are in the pool, its dst is nobody's src and no
@@ -157,19 +161,20 @@ pkv_status pkv_kv_write(const void* k_new, const void* v_new, pkv_dtype in_dtype
   if (in_dtype == cache->kv_dtype) {
     const int chunks = cache->head_dim * dtype_bytes(in_dtype) / 16;
     const int64_t work = int64_t(num_tokens) * cache->num_kv_heads * chunks;
-    kv_write_copy_kernel<<<grid_for(work), kThreads, 0, s>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, cache->num_kv_heads, chunks,
-        cache->block_size, num_slots, err);
+    if (launch_pdl(kv_write_copy_kernel, dim3(grid_for(work)), dim3(kThreads), 0, s,
+                   static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+                   static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_tokens, cache->num_kv_heads,
+                   chunks, cache->block_size, num_slots, err) != cudaSuccess)
+      return PKV_ERR_CUDA;
   } else if (cache->kv_dtype == PKV_FP8_E4M3 && (in_dtype == PKV_F16 || in_dtype == PKV_BF16)) {
     const int chunks = cache->head_dim / 16;
     const int64_t work = int64_t(num_tokens) * cache->num_kv_heads * chunks;
     auto kern = in_dtype == PKV_BF16 ? kv_write_quant_kernel<true> : kv_write_quant_kernel<false>;
-    kern<<<grid_for(work), kThreads, 0, s>>>(static_cast<const uint8_t*>(k_new), static_cast<const uint8_t*>(v_new),
-                                             slot_mapping, static_cast<uint4*>(k_cache),
-                                             static_cast<uint4*>(v_cache), cache->k_scale, cache->v_scale,
-                                             num_tokens, cache->num_kv_heads, chunks, cache->block_size, num_slots,
-                                             err);
+    if (launch_pdl(kern, dim3(grid_for(work)), dim3(kThreads), 0, s, static_cast<const uint8_t*>(k_new),
+                   static_cast<const uint8_t*>(v_new), slot_mapping, static_cast<uint4*>(k_cache),
+                   static_cast<uint4*>(v_cache), cache->k_scale, cache->v_scale, num_tokens, cache->num_kv_heads,
+                   chunks, cache->block_size, num_slots, err) != cudaSuccess)
+      return PKV_ERR_CUDA;
   } else {
     return PKV_ERR_UNSUPPORTED;
   }
@@ -193,9 +198,10 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
       int64_t(cache->num_kv_heads) * cache->block_size * cache->head_dim * dtype_bytes(cache->kv_dtype);
   const int64_t chunks = block_bytes / 16;
   dim3 grid(num_pairs, 2);
-  copy_blocks_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_pairs, num_pairs, cache->num_blocks, chunks,
-      err);
+  if (launch_pdl(copy_blocks_kernel, grid, dim3(kThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+                 static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_pairs, num_pairs,
+                 cache->num_blocks, chunks, err) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

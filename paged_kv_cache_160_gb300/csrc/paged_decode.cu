@@ -271,8 +271,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const Tile c = locate(t);
     return p.block_tables[int64_t(c.s) * p.max_blocks + c.b];
   };
-  int bid_cur = load_window(0);
+  int bid_cur = load_window(0);                // in flight while the piece count below is worked out
   int bid_nxt = n > 32 ? load_window(1) : -1;
+
+  // The only piece of this range that can open a segment without closing it is the
+  // range's last one; the merge needs that segment's piece count.  Worker of unit u: the
+  // largest wi with start_of(wi) <= u, i.e. floor(((u + 1) W - 1) / nunits).  Lengths only,
+  // so it is worked out before the wait.
+  int last_np = 1;
+  if (lane == 0) {
+    const Tile c = locate(t_end - 1);
+    const int64_t u_end = PB ? int64_t(Hkv) * cum_np[c.s] + int64_t(c.h) * (cum_np[c.s + 1] - cum_np[c.s]) +
+                                   (c.nb - 1) / PB
+                             : int64_t(Hkv) * cum_nb[c.s] + int64_t(c.h) * c.nb + c.nb - 1;
+    last_np = int(((u_end + 1) * W - 1) / nunits) - w + 1;
+  }
 
   // Issues the TMA loads of the worker's tile j (cursor c) into stage st; lane 0 records in
   // `valid` (bit st) whether the tile's block id was inside the pool.  Whole warp calls it.
@@ -311,6 +324,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   griddep_wait();
   griddep_launch_dependents();
   zero_empty();
+
+  // The query rows of the segment this range ends in are read only when that piece starts,
+  // late in the range: bring them into L1 now so the switch does not wait on memory.
+  if (t_end - 1 - t_begin >= 1) {
+    const Tile a = locate(t_begin), b = locate(t_end - 1);
+    if (a.s != b.s || a.h != b.h) {
+      const int qbytes = G * D * 2;                      // f16 / bf16 queries
+      const uint8_t* qrow0 = static_cast<const uint8_t*>(p.q) + (int64_t(b.s) * Hkv + b.h) * G * D * 2;
+      for (int off = lane * 128; off < qbytes; off += 32 * 128) prefetch_l1(qrow0 + off);
+    }
+  }
 
   Tile pc = locate(t_begin);                 // producer cursor, kStages tiles ahead
   for (int i = 0; i < min(n, kStages); ++i) {
@@ -503,19 +527,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const bool complete = piece_b0 == 0 && tl.b + 1 == tl.nb;
     if (piece_b0 == 0 && lane == 0) {
       // This worker holds the segment's first tile: describe the segment's pieces for the
-      // merge kernel.  Workers w .. w1 cover it, one piece each; worker w's piece is its
-      // first (slot 2w) if the segment starts its range, else its second (slot 2w + 1).
-      int npieces = 1;
-      if (!complete) {
-        const int64_t last = seg_t0 + tl.nb - 1;
-        auto range_begin = [&](int64_t wi) -> int64_t { return PB ? unit_tile(start_of(wi)) : start_of(wi); };
-        const int64_t guess = last * W / T;
-        int wi = int(guess < W - 1 ? guess : W - 1);
-        while (wi > 0 && range_begin(wi) > last) --wi;
-        while (wi + 1 < W && range_begin(wi + 1) <= last) ++wi;
-        npieces = wi - w + 1;
-      }
-      p.seg_desc[seg] = make_int4(w, npieces, piece_t0 == t_begin ? 0 : 1, 0);
+      // merge kernel.  Workers w .. w + npieces - 1 cover it, one piece each; worker w's
+      // piece is its first (slot 2w) if the segment starts its range, else its second
+      // (slot 2w + 1).  A segment that starts here and runs past the range is the range's
+      // last, whose piece count the prologue worked out.
+      p.seg_desc[seg] = make_int4(w, complete ? 1 : last_np, piece_t0 == t_begin ? 0 : 1, 0);
     }
     if (complete) {
       const float inv0 = ls0 > 0.f ? vs / ls0 : 0.f, inv1 = ls1 > 0.f ? vs / ls1 : 0.f;
@@ -561,52 +577,87 @@ struct MergeParams {
 
 constexpr int kMergeWarps = 8;
 
-// Split-KV merge: one warp per (sequence, query head) whose segment was split.  With
+// Split-KV merge: one warp per (segment, query head) whose segment was split.  With
 // M = max_k m_k over the pieces k,  out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k.
+// Lane k fetches piece k's (m, l) while every lane fetches its 16-byte chunk of up to
+// kChunk pieces' rows; the weights come from warp reductions over the lanes, so the
+// loads of a block of 32 pieces overlap and no exponential sits between a load and the sum.
 template <int QT, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) split_kv_merge_kernel(const MergeParams p) {
   griddep_wait();                            // the decode kernel's partials are complete
+  constexpr int kLanesPerHead = D / 4;       // 16-byte chunks of one head's row
+  constexpr int kHP = 32 / kLanesPerHead;    // rows per load instruction of the warp
+  constexpr int kChunk = 16;                 // loads in flight per lane
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int64_t item = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
   if (item >= int64_t(p.num_segments) * G) return;
   const int seg = int(item / G), hh = int(item % G);
   const int4 d = p.seg_desc[seg];
-  const int w0 = d.x, npieces = d.y;
-  if (npieces <= 1) return;
+  const int w0 = d.x, np = d.y;
+  if (np <= 1) return;
   auto slot_of = [&](int k) -> int64_t { return k == 0 ? 2 * int64_t(w0) + d.z : 2 * int64_t(w0 + k); };
-  // One pass with a running maximum; the loads of different pieces do not depend on each
-  // other, so an unrolled group of pieces is fetched together.
-  constexpr int kVec = D / 32;
-  float acc[kVec];
-#pragma unroll
-  for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
-  float M = -INFINITY, den = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < npieces; ++k) {
-    const int64_t sk = slot_of(k);
-    const float2 ml = p.ml[sk * G + hh];
-    const float* src = p.po + (sk * G + hh) * D + lane * kVec;
-    float v[kVec];
-    if constexpr (kVec == 4) {
-      const float4 t = *reinterpret_cast<const float4*>(src);
-      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-    } else {
-      const float2 t = *reinterpret_cast<const float2*>(src);
-      v[0] = t.x; v[1] = t.y;
+  const int rsub = lane / kLanesPerHead, dof = (lane % kLanesPerHead) * 4;
+  float M = -INFINITY, den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int kb = 0; kb < np; kb += 32) {
+    const int nb = min(32, np - kb);
+    float mk = -INFINITY, lk = 0.f;
+    if (lane < nb) {
+      const float2 t2 = __ldcg(p.ml + slot_of(kb + lane) * G + hh);   // L2: written by the decode grid
+      mk = t2.x;
+      lk = t2.y;
     }
-    if (ml.x == -INFINITY) continue;                       // an empty piece contributes nothing
-    const float Mn = fmaxf(M, ml.x);
-    const float a = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn);   // a = 0 while M = -inf
-    den = den * a + w * ml.y;
+    float wk = 0.f;
+    for (int r0 = 0; r0 < nb; r0 += kChunk * kHP) {
+      float4 v[kChunk];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) acc[e] = acc[e] * a + w * v[e];
-    M = Mn;
+      for (int c = 0; c < kChunk; ++c) {
+        const int r = r0 + c * kHP + rsub;
+        v[c] = r < nb ? __ldcg(reinterpret_cast<const float4*>(p.po + (slot_of(kb + r) * G + hh) * D + dof))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (r0 == 0) {                         // weights of this block, while its rows arrive
+        float mb = mk;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        const float Mn = fmaxf(M, mb);
+        const float Mz = Mn == -INFINITY ? 0.f : Mn;   // every piece so far empty: weights 0
+        const float rescale = fast_exp2(M - Mz);       // 0 while M = -inf
+        wk = fast_exp2(mk - Mz);
+        float lw = lk * wk;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        den = den * rescale + lw;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] *= rescale;
+        M = Mn;
+      }
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const int r = r0 + c * kHP + rsub;
+        const float wr = __shfl_sync(0xffffffffu, wk, r & 31);
+        if (r < nb) {
+          acc[0] += wr * v[c].x;
+          acc[1] += wr * v[c].y;
+          acc[2] += wr * v[c].z;
+          acc[3] += wr * v[c].w;
+        }
+      }
+    }
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  const int64_t obase = (int64_t(seg) * G + hh) * D + lane * kVec;   // out[s][h * G + hh][:]
+  if constexpr (kHP > 1) {                   // fold the rows the half-warps took
 #pragma unroll
-  for (int e = 0; e < kVec; ++e) store_out<QT>(p.out, obase + e, acc[e] * inv);
+    for (int e = 0; e < 4; ++e) {
+#pragma unroll
+      for (int o = kLanesPerHead; o < 32; o <<= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+    }
+  }
+  if (rsub == 0) {
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int64_t obase = (int64_t(seg) * G + hh) * D + dof;   // out[s][h * G + hh][:]
+#pragma unroll
+    for (int e = 0; e < 4; ++e) store_out<QT>(p.out, obase + e, acc[e] * inv);
+  }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -629,29 +680,22 @@ Layout layout(int num_seqs, int num_kv_heads, int group, int head_dim, int64_t s
   return l;
 }
 
-constexpr size_t kSmemLimit = 227 * 1024;
+// Dynamic shared memory a launch of `kern` may request: the device's per-CTA opt-in limit
+// less the kernel's static arrays.
+template <typename K>
+size_t dynamic_smem_limit(K kern) {
+  int dev = 0, optin = 0;
+  cudaFuncAttributes fa = {};
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, kern) != cudaSuccess || size_t(optin) <= fa.sharedSizeBytes)
+    return 0;
+  return size_t(optin) - fa.sharedSizeBytes;
+}
 
 template <int KV, int D, int NW, int NS>
 size_t smem_bytes(int num_seqs) {
   return 1024 + size_t(NW) * NS * Cfg<KV, D>::kStageBytes + 2 * sizeof(int) * size_t(num_seqs + 1);
-}
-
-// Launch with programmatic stream serialization: the kernel may be scheduled while the
-// previous kernel on the stream runs, and waits for it in griddep_wait().
-template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 template <int KV, int QT, int D, int NW, int NS>
@@ -682,9 +726,18 @@ pkv_status launch_cfg(DecodeParams prm, const CUtensorMap& tk, const CUtensorMap
 template <int KV, int QT, int D>
 pkv_status launch(const DecodeParams& prm, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                   cudaStream_t stream) {
-  if (smem_bytes<KV, D, kMaxWarps, 2>(prm.num_seqs) <= kSmemLimit)
+  static thread_local int cached_dev = -1;
+  static thread_local size_t lim12 = 0, lim4 = 0;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev != cached_dev) {                   // looked up once per device and thread
+    lim12 = dynamic_smem_limit(paged_decode_kernel<KV, QT, D, kMaxWarps, 2>);
+    lim4 = dynamic_smem_limit(paged_decode_kernel<KV, QT, D, 4, 2>);
+    cached_dev = dev;
+  }
+  if (smem_bytes<KV, D, kMaxWarps, 2>(prm.num_seqs) <= lim12)
     return launch_cfg<KV, QT, D, kMaxWarps, 2>(prm, tk, tv, grid, stream);
-  if (smem_bytes<KV, D, 4, 2>(prm.num_seqs) <= kSmemLimit) return launch_cfg<KV, QT, D, 4, 2>(prm, tk, tv, grid, stream);
+  if (smem_bytes<KV, D, 4, 2>(prm.num_seqs) <= lim4) return launch_cfg<KV, QT, D, 4, 2>(prm, tk, tv, grid, stream);
   return PKV_ERR_UNSUPPORTED;
 }
 

@@ -1,6 +1,8 @@
 // Host-side helpers shared by the libpkv entry points (not part of the public ABI).
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,5 +36,26 @@ inline int dtype_bytes(pkv_dtype d) { return d == PKV_FP8_E4M3 ? 1 : 2; }
 
 // Shared checks of a cache descriptor; returns PKV_OK or the failing status.
 pkv_status check_cache_desc(const pkv_cache_desc* c);
+
+#ifdef __CUDACC__
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel on the stream still runs, and must call griddep_wait() before it touches
+// memory that kernel may write.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+#endif
 
 }  // namespace pkv

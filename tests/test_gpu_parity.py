@@ -103,6 +103,8 @@ SMALL = [
     ("gqa3_f16", [2, 64, 65, 129], 6, 2, 128, "f16", "f16", 64),
     ("e4m3_bf16q", [1, 17, 511, 512, 513, 2000], 32, 8, 128, "bf16", "e4m3", 512),
     ("e4m3_f16q_balanced", [7, 16, 130, 900], 8, 2, 128, "f16", "e4m3", 0),
+    # six workers in one CTA merge sixteen (segment, head) items
+    ("few_workers_gqa8", [80, 80], 8, 1, 128, "bf16", "bf16", 32),
     ("gqa5_many_seqs", [int(x) for x in np.random.default_rng(5).integers(1, 80, size=300)], 10, 2, 128,
      "bf16", "bf16", 0),
 ]
@@ -112,6 +114,16 @@ SMALL = [
 def test_small_cases(name, lens, hq, hkv, d, qd, kd, part):
     case = synth.make_decode_case(name, 77, lens, hq, hkv, d, qd, kd, partition_size=part)
     _check_case(case)
+
+
+def test_very_large_batch_takes_the_four_warp_layout():
+    """4500 sequences: the per-sequence prefix arrays no longer fit beside twelve warps'
+    stages, so the kernel runs with four worker warps per CTA; sampled rows vs the oracle."""
+    rng = np.random.default_rng(6)
+    lens = [int(x) for x in rng.integers(1, 40, size=4500)]
+    case = synth.make_decode_case("huge_batch", 82, lens, 4, 1, 128, "bf16", "bf16")
+    rows = sorted({(int(s), int(h)) for s, h in zip(rng.integers(0, 4500, 300), rng.integers(0, 4, 300))})
+    _check_case(case, decode_rows=rows, compare_caches=False)
 
 
 @pytest.mark.parametrize("kd", ["bf16", "e4m3"])
