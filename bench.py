@@ -5,7 +5,8 @@ lengths uniform in [128, 2048], 28 query heads / 4 kv heads, head_dim 128, bf16 
 16-token blocks in a shuffled pool ([num_blocks, 4, 16, 128], pool = blocks needed + 10%).
 One step = plan the step on the host block manager (done once; its cost is reported
 separately), kv_write of the 64 new tokens, then paged_decode over every sequence's
-L + 1 tokens (one launch: split-KV and merge).
+L + 1 tokens (two launches: the split-KV decode, then the log-sum-exp merge of split
+segments as its programmatic dependent).
 
 Timing: CUDA events on the launching stream.  The K timed steps are captured into one
 CUDA graph and replayed once between two events.  The decode kernel's own average duration
@@ -44,10 +45,11 @@ WORKLOAD = ("qwen2.5-7b-gqa paged decode step: 64 seqs, context_lens U[128,2048]
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes per paged_decode launch on this workload from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel source with
-# this hash; when the source changes, traffic is reported as null until re-measured.
-TRAFFIC = {"source_sha1": "1be57afd78389a70cc8243eaa99ed48069e3ae28", "bytes_per_launch": 154050048}
+# DRAM bytes per decode call on this workload (paged_decode_kernel + split_kv_merge_kernel,
+# dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture each), valid only for the
+# kernel source with this hash; when the source changes, traffic is reported as null until
+# re-measured.
+TRAFFIC = {"source_sha1": "382d42d9e8101985bf6f523f077974a7cae5b71e", "bytes_per_launch": 161459712}
 
 
 def _src_hash() -> str:
