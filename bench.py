@@ -317,6 +317,7 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     assert torch.equal(h_out.to(dev), out)
     pf_ms, pf_flops = prefill_measure(dev)
+    sw_out, sw_in, sw_bytes = swap_measure(dev)
 
     peak, peak_kind = _peaks()
     ms_per_step = elapsed_ms / K
@@ -358,6 +359,9 @@ def run_gpu(args):
                           "peak": _bf16_peak(), "unit": "TFLOP/s",
                           "frac": round(pf_flops / (pf_ms * 1e-3) / 1e12 / _bf16_peak(), 4),
                           "avg_launch_ms": round(pf_ms, 5), "flops_per_launch": pf_flops},
+        "swap_blocks": {"workload": "4096 scattered blocks of the 7B layout (K and V), device <-> pinned host",
+                        "bytes_per_call": sw_bytes, "device_to_host_gbs": round(sw_out, 1),
+                        "host_to_device_gbs": round(sw_in, 1)},
         "host_plan_us": round(host_plan_us, 1),
         "gpu_launches": 3 * K,                       # kv_write, decode, merge per timed step
         "clocks": clk.summary(),
@@ -416,6 +420,40 @@ def prefill_measure(dev, iters: int = 30):
     pairs = sum(ch.prefix_len + r + 1 for r in range(ch.q_len))
     flops = 4 * case.head_dim * pairs * case.num_heads
     return ms, flops
+
+
+def swap_measure(dev, n_blocks: int = 4096, iters: int = 10):
+    """pkv_swap_blocks between the device pool and a pinned host pool, 7B-workload block layout
+    ([blocks, 4 kv heads, 16, 128] bf16: 16 KiB per K or V block), blocks scattered by a
+    permutation.  Returns (device->host GB/s, host->device GB/s, bytes per call)."""
+    import torch
+    import paged_kv_cache_160_gb300 as pkv
+    g = torch.Generator(device=dev).manual_seed(7)
+    shape = (n_blocks, 4, 16, 128)
+    kc = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+    vc = torch.randn(shape, device=dev, generator=g).to(torch.bfloat16)
+    hk = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+    desc = pkv.cache_desc(kc)
+    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(8))
+    out_pairs = torch.stack([torch.arange(n_blocks), perm], 1).to(torch.int32).to(dev)
+    in_pairs = torch.stack([perm, torch.arange(n_blocks)], 1).to(torch.int32).to(dev)
+    s = torch.cuda.Stream(device=dev)
+    res = []
+    for dst_k, dst_v, src_k, src_v, pairs in ((hk, hv, kc, vc, out_pairs), (kc, vc, hk, hv, in_pairs)):
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                pkv.pkv_swap_blocks(dst_k, dst_v, src_k, src_v, desc, pairs, s)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(iters):
+                pkv.pkv_swap_blocks(dst_k, dst_v, src_k, src_v, desc, pairs, s)
+            b.record(s)
+        s.synchronize()
+        res.append(a.elapsed_time(b) / iters)
+    assert pkv.pkv_get_device_error(s) == 0
+    nbytes = 2 * kc.numel() * kc.element_size()
+    return nbytes / (res[0] * 1e-3) / 1e9, nbytes / (res[1] * 1e-3) / 1e9, nbytes
 
 
 def _oracle_step(case, plan, seqs):

@@ -119,6 +119,26 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache
                            const int32_t* block_pairs, int num_pairs, pkv_stream_t stream);
 
 /*
+ * swap_blocks: preemption by swapping ("Lecture 33 — KV Cache management" §5.2: the
+ * victim's blocks are copied to host RAM, its device blocks are released, and later the
+ * blocks are copied back so the sequence can resume).  Block copies between two pools of
+ * the same block layout: num_kv_heads, block_size, head_dim and kv_dtype come from `layout`
+ * (its num_blocks is not used).  Either pool may be pinned host memory (cudaHostAlloc /
+ * cudaHostRegister), passed by its device-visible address (with unified addressing, the
+ * host pointer itself).
+ *   dst_k/dst_v, src_k/src_v  [num_blocks][num_kv_heads][block_size][head_dim] each
+ *   dst_num_blocks, src_num_blocks  pool sizes in blocks (ids are checked against them)
+ *   block_pairs (device) int32 [num_pairs][2] = (src block, dst block)
+ * For each pair, block dst of dst_k (and dst_v) becomes a copy of block src of src_k
+ * (src_v).  Pairs with an id outside its pool, or whose dst another pair also names, are
+ * skipped and flagged PKV_DEVERR_COPY_PAIR.  pkv_bm_swap_out / pkv_bm_swap_in produce the
+ * pairs.  Launched like kv_write (programmatic dependent, waits before touching memory).
+ */
+PKV_API pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks, const void* src_k,
+                                   const void* src_v, int src_num_blocks, const pkv_cache_desc* layout,
+                                   const int32_t* block_pairs, int num_pairs, pkv_stream_t stream);
+
+/*
  * Workspace bytes pkv_paged_decode needs on the current device: two partial-result
  * slots per worker warp (running max, sum of exponentials and unnormalised output per
  * query head) plus one piece descriptor per (sequence, kv head).  It depends on the
@@ -272,6 +292,30 @@ PKV_API pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq);
 /* tables int32 [n][max_blocks] (padded with -1), lens int32 [n]. */
 PKV_API pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n, int max_blocks,
                          int32_t* tables, int32_t* lens);
+
+/* Preemption by swapping ("Lecture 33 — KV Cache management" §5.2).  The host pool is a
+ * second set of num_host_blocks blocks (ids 0..num_host_blocks-1 of a caller-owned pinned
+ * buffer with the device pool's block layout) with its own FIFO free queue.  Resizing is
+ * allowed only while no sequence is swapped out; the queue restarts as 0..n-1. */
+PKV_API pkv_status pkv_bm_set_host_pool(pkv_block_manager* bm, int num_host_blocks);
+
+/* Swap a resident sequence out: for each table entry in order a host block is popped and
+ * pairs[i] = (device block, host block); then the device blocks are released in table order
+ * (ref_cnt - 1, free at 0), as by pkv_bm_free.  A block shared with another sequence stays on
+ * the device for it; this sequence takes its own host copy.  Until swapped in, the sequence
+ * can only be freed or swapped in (other calls on it return PKV_ERR_INVALID_ARG).
+ *   pairs int32 [max_pairs][2]; *n_pairs = number of table entries.
+ * PKV_ERR_NO_BLOCKS, changing nothing, if the host queue holds fewer blocks than the table. */
+PKV_API pkv_status pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq, int32_t* pairs, int max_pairs,
+                                   int* n_pairs);
+
+/* Swap a sequence back in: for each host block in table order a device block is popped and
+ * pairs[i] = (host block, device block); the host blocks return to the host queue's tail in
+ * table order.  PKV_ERR_NO_BLOCKS, changing nothing, if too few device blocks are free. */
+PKV_API pkv_status pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq, int32_t* pairs, int max_pairs,
+                                  int* n_pairs);
+PKV_API int pkv_bm_num_free_host(const pkv_block_manager* bm);
+PKV_API int pkv_bm_is_swapped(const pkv_block_manager* bm, int64_t seq);   /* 1, 0, or -1 if unknown */
 
 PKV_API int pkv_bm_ref_cnt(const pkv_block_manager* bm, int block);      /* -1 if out of range */
 PKV_API int pkv_bm_num_free(const pkv_block_manager* bm);

@@ -12,7 +12,10 @@ Sources:
 * "Lecture 33 — KV Cache management", §2.2 (per-sequence block table, slot address)
   and §2.4 (fork copies only the table and raises each block's count; a write into a
   block whose count is above 1 first takes a new block, copies the old block into
-  it, points the writer's table at it and lowers the old block's count).
+  it, points the writer's table at it and lowers the old block's count).  §5.2
+  (preemption by swapping): the victim's blocks are copied to host memory, its device
+  blocks are released for the others, and when memory frees up the blocks are copied
+  back and the sequence resumes.
 
 Readings where the pages are silent:
 
@@ -20,6 +23,12 @@ Readings where the pages are silent:
 * ``import_seq`` claims named blocks directly (used to set up synthetic states such
   as two sequences sharing a block); a claimed free block leaves the free queue.
 * Running out of free blocks raises ``NoBlocks`` and leaves the state unchanged.
+* Swapping: the host swap space is a second pool of blocks with its own FIFO queue.
+  Swap-out gives each table entry, in order, a host block, then releases the device
+  blocks in table order exactly as ``free`` does (a block shared with another
+  sequence stays for it; the swapped sequence takes its own host copy).  Swap-in pops
+  one device block per table entry in order and returns the host blocks to the host
+  queue's tail in table order.  A swapped sequence can only be freed or swapped in.
 """
 from __future__ import annotations
 
@@ -47,6 +56,8 @@ class BlockManagerModel:
         self.ref_cnt = [0] * num_blocks
         self.tables: Dict[int, List[int]] = {}
         self.num_tokens: Dict[int, int] = {}
+        self.host_free: deque = deque()
+        self.swapped: Dict[int, bool] = {}
 
     # -- pool ---------------------------------------------------------------------------
     def num_free(self) -> int:
@@ -92,9 +103,14 @@ class BlockManagerModel:
         self.tables[seq] = [self._pop() for _ in range(need)]
         self.num_tokens[seq] = n_tokens
 
+    def _resident(self, seq: int) -> List[int]:
+        if seq not in self.tables or self.swapped.get(seq):
+            raise InvalidArg("not a resident sequence")
+        return self.tables[seq]
+
     def append_slot(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
         """Reserve the slot of the sequence's next token; returns (slot, cow_pair or None)."""
-        table = self.tables[seq]
+        table = self._resident(seq)
         p = self.num_tokens[seq]
         bs = self.block_size
         cow = None
@@ -112,6 +128,7 @@ class BlockManagerModel:
 
     def append_slots(self, seq: int, n: int) -> Tuple[List[int], List[Tuple[int, int]]]:
         """``n`` consecutive append_slot calls; all of them or none (state restored on NoBlocks)."""
+        self._resident(seq)
         saved = (deque(self.free_queue), list(self.ref_cnt), {k: list(v) for k, v in self.tables.items()},
                  dict(self.num_tokens))
         slots, cows = [], []
@@ -129,21 +146,56 @@ class BlockManagerModel:
     def fork(self, parent: int, child: int) -> None:
         if child in self.tables:
             raise InvalidArg("sequence exists")
-        self.tables[child] = list(self.tables[parent])
+        self.tables[child] = list(self._resident(parent))
         self.num_tokens[child] = self.num_tokens[parent]
         for b in self.tables[child]:
             self.ref_cnt[b] += 1
 
     def free(self, seq: int) -> None:
-        for b in self.tables.pop(seq):
-            self._release(b)
+        if self.swapped.pop(seq, False):
+            self.host_free.extend(self.tables.pop(seq))
+        else:
+            for b in self.tables.pop(seq):
+                self._release(b)
         del self.num_tokens[seq]
+
+    # -- swapping ------------------------------------------------------------------------
+    def set_host_pool(self, num_host_blocks: int) -> None:
+        if any(self.swapped.values()):
+            raise InvalidArg("a sequence is swapped out")
+        self.host_free = deque(range(num_host_blocks))
+
+    def swap_out(self, seq: int) -> List[Tuple[int, int]]:
+        if self.swapped.get(seq) or seq not in self.tables:
+            raise InvalidArg("not a resident sequence")
+        table = self.tables[seq]
+        if len(table) > len(self.host_free):
+            raise NoBlocks("host swap space is full")
+        host = [self.host_free.popleft() for _ in table]
+        pairs = list(zip(table, host))
+        for b in table:
+            self._release(b)
+        self.tables[seq] = host
+        self.swapped[seq] = True
+        return pairs
+
+    def swap_in(self, seq: int) -> List[Tuple[int, int]]:
+        if not self.swapped.get(seq):
+            raise InvalidArg("not swapped out")
+        host = self.tables[seq]
+        if len(host) > len(self.free_queue):
+            raise NoBlocks("not enough free device blocks")
+        dev = [self._pop() for _ in host]
+        self.host_free.extend(host)
+        self.tables[seq] = dev
+        self.swapped[seq] = False
+        return list(zip(host, dev))
 
     def export(self, seqs: Sequence[int], max_blocks: int) -> Tuple[List[List[int]], List[int]]:
         """Block tables padded with -1 to ``max_blocks`` and the token counts."""
         tables, lens = [], []
         for s in seqs:
-            t = self.tables[s]
+            t = self._resident(s)
             if len(t) > max_blocks:
                 raise InvalidArg("table longer than max_blocks")
             tables.append(t + [-1] * (max_blocks - len(t)))

@@ -7,7 +7,8 @@ Sources:
   tokens are written to the cache as well ("Lecture 33", §4.2).
 * "Lecture 33 — KV Cache management", §2.2 (slot = physical block * block_size +
   offset) and §2.4 (copy-on-write: the writer gets a new block holding a copy of the
-  shared block's contents).
+  shared block's contents); §5.2 (swapping: a preempted sequence's blocks are copied to
+  host memory and later copied back).
 
 Reading where the pages are silent: a negative slot marks a padding token and is
 skipped.  Caches are the stored codes, layout ``[num_blocks, num_kv_heads,
@@ -47,4 +48,18 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray,
     for src, dst in pairs:
         k_out[int(dst)] = k_cache[int(src)]
         v_out[int(dst)] = v_cache[int(src)]
+    return k_out, v_out
+
+
+def swap_blocks(dst_k: np.ndarray, dst_v: np.ndarray, src_k: np.ndarray, src_v: np.ndarray,
+                pairs: Sequence[Tuple[int, int]]) -> Tuple[np.ndarray, np.ndarray]:
+    """For each (src, dst): block ``dst`` of the destination pool becomes a copy of block
+    ``src`` of the source pool (the two pools share the block layout; one of them is the
+    host swap space).  No dst may repeat."""
+    dsts = [int(d) for _, d in pairs]
+    assert len(set(dsts)) == len(dsts), "a dst block repeats"
+    k_out, v_out = dst_k.copy(), dst_v.copy()
+    for src, dst in pairs:
+        k_out[int(dst)] = src_k[int(src)]
+        v_out[int(dst)] = src_v[int(src)]
     return k_out, v_out

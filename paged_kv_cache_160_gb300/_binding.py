@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 from ctypes import POINTER, c_float, c_int, c_int32, c_int64, c_size_t, c_void_p
-from typing import Optional, Sequence, Tuple
+from typing import List, Optional, Sequence, Tuple
 
 import torch
 
@@ -51,6 +51,9 @@ def _load() -> ctypes.CDLL:
                                  POINTER(CacheDesc), c_void_p]
     lib.pkv_copy_blocks.restype = S
     lib.pkv_copy_blocks.argtypes = [c_void_p, c_void_p, POINTER(CacheDesc), c_void_p, c_int, c_void_p]
+    lib.pkv_swap_blocks.restype = S
+    lib.pkv_swap_blocks.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, POINTER(CacheDesc),
+                                    c_void_p, c_int, c_void_p]
     lib.pkv_decode_workspace_bytes.restype = c_size_t
     lib.pkv_decode_workspace_bytes.argtypes = [c_int] * 7
     lib.pkv_paged_decode.restype = S
@@ -92,6 +95,16 @@ def _load() -> ctypes.CDLL:
     lib.pkv_bm_free.argtypes = [BM, c_int64]
     lib.pkv_bm_export.restype = S
     lib.pkv_bm_export.argtypes = [BM, POINTER(c_int64), c_int, c_int, POINTER(c_int32), POINTER(c_int32)]
+    lib.pkv_bm_set_host_pool.restype = S
+    lib.pkv_bm_set_host_pool.argtypes = [BM, c_int]
+    lib.pkv_bm_swap_out.restype = S
+    lib.pkv_bm_swap_out.argtypes = [BM, c_int64, POINTER(c_int32), c_int, POINTER(c_int)]
+    lib.pkv_bm_swap_in.restype = S
+    lib.pkv_bm_swap_in.argtypes = [BM, c_int64, POINTER(c_int32), c_int, POINTER(c_int)]
+    lib.pkv_bm_num_free_host.restype = c_int
+    lib.pkv_bm_num_free_host.argtypes = [BM]
+    lib.pkv_bm_is_swapped.restype = c_int
+    lib.pkv_bm_is_swapped.argtypes = [BM, c_int64]
     lib.pkv_bm_ref_cnt.restype = c_int
     lib.pkv_bm_ref_cnt.argtypes = [BM, c_int]
     lib.pkv_bm_num_free.restype = c_int
@@ -171,6 +184,26 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, desc: CacheDes
     _check(lib.pkv_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
                                _dev(block_pairs, "block_pairs"), block_pairs.shape[0], _stream(stream)),
            "pkv_copy_blocks")
+
+
+def _dev_or_pinned(t: torch.Tensor, name: str) -> int:
+    """Device address of a CUDA tensor, or of a pinned host tensor (unified addressing)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def pkv_swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor,
+                    desc: CacheDesc, block_pairs: torch.Tensor, stream=None) -> None:
+    """Block copies between two pools of ``desc``'s layout; either may be pinned host memory."""
+    assert block_pairs.dtype == torch.int32
+    _check(lib.pkv_swap_blocks(_dev_or_pinned(dst_k, "dst_k"), _dev_or_pinned(dst_v, "dst_v"), dst_k.shape[0],
+                               _dev_or_pinned(src_k, "src_k"), _dev_or_pinned(src_v, "src_v"), src_k.shape[0],
+                               ctypes.byref(desc), _dev(block_pairs, "block_pairs"), block_pairs.shape[0],
+                               _stream(stream)),
+           "pkv_swap_blocks")
 
 
 def pkv_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
@@ -289,6 +322,29 @@ class BlockManager:
 
     def free(self, seq: int) -> None:
         _check(lib.pkv_bm_free(self._h, seq), "pkv_bm_free")
+
+    def set_host_pool(self, num_host_blocks: int) -> None:
+        _check(lib.pkv_bm_set_host_pool(self._h, num_host_blocks), "pkv_bm_set_host_pool")
+
+    def _swap(self, fn, name, seq: int, max_pairs: int):
+        pairs = (c_int32 * max(1, 2 * max_pairs))()
+        n = c_int()
+        _check(fn(self._h, seq, pairs, max_pairs, ctypes.byref(n)), name)
+        return [(pairs[2 * i], pairs[2 * i + 1]) for i in range(n.value)]
+
+    def swap_out(self, seq: int, max_pairs: int = 1 << 16) -> List[Tuple[int, int]]:
+        """(device block, host block) pairs, in table order."""
+        return self._swap(lib.pkv_bm_swap_out, "pkv_bm_swap_out", seq, max_pairs)
+
+    def swap_in(self, seq: int, max_pairs: int = 1 << 16) -> List[Tuple[int, int]]:
+        """(host block, device block) pairs, in table order."""
+        return self._swap(lib.pkv_bm_swap_in, "pkv_bm_swap_in", seq, max_pairs)
+
+    def num_free_host(self) -> int:
+        return lib.pkv_bm_num_free_host(self._h)
+
+    def is_swapped(self, seq: int) -> int:
+        return lib.pkv_bm_is_swapped(self._h, seq)
 
     def export(self, seqs: Sequence[int], max_blocks: int):
         n = len(seqs)

@@ -1,12 +1,14 @@
 // Host block manager: the free-block queue, per-block ref_cnt and per-sequence block
 // tables of "PagedAttention: manage the KV cache like virtual memory" §3.2–§3.3, with
-// fork and copy-on-write from "Lecture 33 — KV Cache management" §2.4.
+// fork and copy-on-write from "Lecture 33 — KV Cache management" §2.4 and preemption by
+// swapping (a host-memory block pool with its own FIFO queue) from its §5.2.
 //
 // The free queue is an intrusive doubly linked list over block ids (allocate pops the
 // head, free pushes the tail, a claimed block is unlinked from the middle in O(1)).
 // Every entry point validates first and mutates after, so a failing call leaves the
 // manager unchanged.
 #include <cstdint>
+#include <deque>
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
@@ -17,8 +19,9 @@
 namespace {
 
 struct Seq {
-  std::vector<int32_t> blocks;
+  std::vector<int32_t> blocks;   // device blocks, or host blocks while swapped out
   int64_t n_tokens = 0;
+  bool swapped = false;
 };
 
 }  // namespace
@@ -32,6 +35,15 @@ struct pkv_block_manager {
   int32_t head = -1, tail = -1;
   int num_free = 0;
   std::unordered_map<int64_t, Seq> seqs;
+  std::deque<int32_t> host_free;     // host swap pool: FIFO of free host block ids
+  int num_host_blocks = 0;
+  int num_swapped = 0;
+
+  // A resident (not swapped out) sequence, or nullptr.
+  Seq* resident(int64_t seq) {
+    auto it = seqs.find(seq);
+    return it == seqs.end() || it->second.swapped ? nullptr : &it->second;
+  }
 
   void push_tail(int32_t b) {
     prev[b] = tail;
@@ -144,19 +156,19 @@ pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq, int n_tokens) {
 pkv_status pkv_bm_append_slot(pkv_block_manager* bm, int64_t seq, int64_t* slot, int32_t* cow_src,
                               int32_t* cow_dst) {
   if (!bm || !slot || !cow_src || !cow_dst) return PKV_ERR_INVALID_ARG;
-  auto it = bm->seqs.find(seq);
-  if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
-  if (bm->pops_for_append(it->second, it->second.n_tokens, nullptr) > bm->num_free) return PKV_ERR_NO_BLOCKS;
-  *slot = bm->append(it->second, cow_src, cow_dst);
+  Seq* sq = bm->resident(seq);
+  if (!sq) return PKV_ERR_INVALID_ARG;
+  if (bm->pops_for_append(*sq, sq->n_tokens, nullptr) > bm->num_free) return PKV_ERR_NO_BLOCKS;
+  *slot = bm->append(*sq, cow_src, cow_dst);
   return PKV_OK;
 }
 
 pkv_status pkv_bm_append_slots(pkv_block_manager* bm, int64_t seq, int n, int64_t* slots, int32_t* cow_pairs,
                                int* n_cow) {
   if (!bm || n < 0 || (n > 0 && (!slots || !cow_pairs)) || !n_cow) return PKV_ERR_INVALID_ARG;
-  auto it = bm->seqs.find(seq);
-  if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
-  Seq& s = it->second;
+  Seq* sq = bm->resident(seq);
+  if (!sq) return PKV_ERR_INVALID_ARG;
+  Seq& s = *sq;
   // Pops needed: a copy-on-write of the current last block (if shared and partially
   // filled) plus one block per block boundary crossed.
   int64_t need = 0;
@@ -192,9 +204,9 @@ pkv_status pkv_bm_step_decode(pkv_block_manager* bm, const int64_t* seqs, int n,
   std::unordered_map<int32_t, int> drop;
   int64_t need = 0;
   for (int i = 0; i < n; ++i) {
-    auto it = bm->seqs.find(seqs[i]);
-    if (it == bm->seqs.end() || !seen.insert(seqs[i]).second) return PKV_ERR_INVALID_ARG;
-    const Seq& s = it->second;
+    const Seq* sq = bm->resident(seqs[i]);
+    if (!sq || !seen.insert(seqs[i]).second) return PKV_ERR_INVALID_ARG;
+    const Seq& s = *sq;
     if (bm->blocks_for(s.n_tokens + 1) > max_blocks) return PKV_ERR_INVALID_ARG;
     int pops = bm->pops_for_append(s, s.n_tokens, &drop);
     if (pops && s.n_tokens % bm->block_size != 0) ++drop[s.blocks[s.n_tokens / bm->block_size]];
@@ -218,9 +230,9 @@ pkv_status pkv_bm_step_decode(pkv_block_manager* bm, const int64_t* seqs, int n,
 
 pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child) {
   if (!bm) return PKV_ERR_INVALID_ARG;
-  auto it = bm->seqs.find(parent);
-  if (it == bm->seqs.end() || bm->seqs.count(child)) return PKV_ERR_INVALID_ARG;
-  Seq c = it->second;
+  const Seq* ps = bm->resident(parent);
+  if (!ps || bm->seqs.count(child)) return PKV_ERR_INVALID_ARG;
+  Seq c = *ps;
   for (int32_t b : c.blocks) ++bm->ref[b];
   bm->seqs.emplace(child, std::move(c));
   return PKV_OK;
@@ -230,7 +242,12 @@ pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq) {
   if (!bm) return PKV_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PKV_ERR_INVALID_ARG;
-  for (int32_t b : it->second.blocks) bm->release(b);
+  if (it->second.swapped) {                  // its host blocks go back to the host queue
+    for (int32_t b : it->second.blocks) bm->host_free.push_back(b);
+    --bm->num_swapped;
+  } else {
+    for (int32_t b : it->second.blocks) bm->release(b);
+  }
   bm->seqs.erase(it);
   return PKV_OK;
 }
@@ -241,7 +258,8 @@ pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n
   if (n > 0 && (!seqs || !tables || !lens)) return PKV_ERR_INVALID_ARG;
   for (int i = 0; i < n; ++i) {
     auto it = bm->seqs.find(seqs[i]);
-    if (it == bm->seqs.end() || int64_t(it->second.blocks.size()) > max_blocks) return PKV_ERR_INVALID_ARG;
+    if (it == bm->seqs.end() || it->second.swapped || int64_t(it->second.blocks.size()) > max_blocks)
+      return PKV_ERR_INVALID_ARG;
     if (it->second.n_tokens > INT32_MAX) return PKV_ERR_INVALID_ARG;
   }
   for (int i = 0; i < n; ++i) {
@@ -253,6 +271,68 @@ pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n
     lens[i] = int32_t(s.n_tokens);
   }
   return PKV_OK;
+}
+
+pkv_status pkv_bm_set_host_pool(pkv_block_manager* bm, int num_host_blocks) {
+  if (!bm || num_host_blocks < 0 || bm->num_swapped > 0) return PKV_ERR_INVALID_ARG;
+  bm->num_host_blocks = num_host_blocks;
+  bm->host_free.clear();
+  for (int b = 0; b < num_host_blocks; ++b) bm->host_free.push_back(b);
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_swap_out(pkv_block_manager* bm, int64_t seq, int32_t* pairs, int max_pairs, int* n_pairs) {
+  if (!bm || !n_pairs || max_pairs < 0) return PKV_ERR_INVALID_ARG;
+  Seq* sq = bm->resident(seq);
+  if (!sq || int64_t(sq->blocks.size()) > max_pairs || (!sq->blocks.empty() && !pairs)) return PKV_ERR_INVALID_ARG;
+  if (sq->blocks.size() > bm->host_free.size()) return PKV_ERR_NO_BLOCKS;
+  // Each table entry gets a host block (in table order); then the device blocks are released
+  // in table order, as if the sequence were freed.  A block shared with another sequence
+  // stays on the device for it; this sequence takes its own host copy.
+  std::vector<int32_t> host(sq->blocks.size());
+  for (size_t i = 0; i < sq->blocks.size(); ++i) {
+    host[i] = bm->host_free.front();
+    bm->host_free.pop_front();
+    pairs[2 * i] = sq->blocks[i];
+    pairs[2 * i + 1] = host[i];
+  }
+  for (int32_t b : sq->blocks) bm->release(b);
+  sq->blocks = std::move(host);
+  sq->swapped = true;
+  ++bm->num_swapped;
+  *n_pairs = int(sq->blocks.size());
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_swap_in(pkv_block_manager* bm, int64_t seq, int32_t* pairs, int max_pairs, int* n_pairs) {
+  if (!bm || !n_pairs || max_pairs < 0) return PKV_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end() || !it->second.swapped) return PKV_ERR_INVALID_ARG;
+  Seq& s = it->second;
+  if (int64_t(s.blocks.size()) > max_pairs || (!s.blocks.empty() && !pairs)) return PKV_ERR_INVALID_ARG;
+  if (int64_t(s.blocks.size()) > bm->num_free) return PKV_ERR_NO_BLOCKS;
+  // Each host block gets a fresh device block (popped in table order); the host blocks
+  // return to the tail of the host queue in table order.
+  std::vector<int32_t> dev(s.blocks.size());
+  for (size_t i = 0; i < s.blocks.size(); ++i) {
+    dev[i] = bm->pop_head();
+    pairs[2 * i] = s.blocks[i];
+    pairs[2 * i + 1] = dev[i];
+  }
+  for (int32_t b : s.blocks) bm->host_free.push_back(b);
+  s.blocks = std::move(dev);
+  s.swapped = false;
+  --bm->num_swapped;
+  *n_pairs = int(s.blocks.size());
+  return PKV_OK;
+}
+
+int pkv_bm_num_free_host(const pkv_block_manager* bm) { return bm ? int(bm->host_free.size()) : -1; }
+
+int pkv_bm_is_swapped(const pkv_block_manager* bm, int64_t seq) {
+  if (!bm) return -1;
+  auto it = bm->seqs.find(seq);
+  return it == bm->seqs.end() ? -1 : (it->second.swapped ? 1 : 0);
 }
 
 int pkv_bm_ref_cnt(const pkv_block_manager* bm, int block) {

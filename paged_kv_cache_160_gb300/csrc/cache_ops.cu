@@ -126,6 +126,43 @@ __global__ void __launch_bounds__(kThreads) copy_blocks_kernel(uint4* __restrict
   for (int64_t i = threadIdx.x; i < chunks; i += blockDim.x) d[i] = s[i];
 }
 
+// One CTA per (pair, K or V) between two pools of the same block layout, either of which may
+// be pinned host memory (Grace reaches it over NVLink-C2C).  Each thread keeps four 16-byte
+// loads in flight, so a block is read with few round trips even from host memory.
+__global__ void __launch_bounds__(kThreads) swap_blocks_kernel(uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                                                               const uint4* __restrict__ src_k,
+                                                               const uint4* __restrict__ src_v,
+                                                               const int32_t* __restrict__ pairs, int num_pairs,
+                                                               int src_blocks, int dst_blocks, int64_t chunks,
+                                                               unsigned* err) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int pair = blockIdx.x;
+  const int32_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+  // Applied only when both ids are inside their pools and no other pair writes the same dst.
+  bool bad = src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks;
+  for (int j = threadIdx.x; j < num_pairs && !bad; j += blockDim.x) {
+    if (j != pair && pairs[2 * j + 1] == dst) bad = true;
+  }
+  bad = __syncthreads_or(bad);
+  if (bad) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_error(err, PKV_DEVERR_COPY_PAIR);
+    return;
+  }
+  const uint4* sp = (blockIdx.y == 0 ? src_k : src_v) + int64_t(src) * chunks;
+  uint4* dp = (blockIdx.y == 0 ? dst_k : dst_v) + int64_t(dst) * chunks;
+  constexpr int kUnroll = 4;
+  int64_t i = threadIdx.x;
+  for (; i + (kUnroll - 1) * int64_t(blockDim.x) < chunks; i += kUnroll * int64_t(blockDim.x)) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = sp[i + u * int64_t(blockDim.x)];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) dp[i + u * int64_t(blockDim.x)] = v[u];
+  }
+  for (; i < chunks; i += blockDim.x) dp[i] = sp[i];
+}
+
 // One 16-byte chunk per thread: these kernels are latency-bound at serving sizes, so every
 // thread should issue its loads once rather than loop.
 int grid_for(int64_t work) {
@@ -203,6 +240,31 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
                  cache->num_blocks, chunks, err) != cudaSuccess)
     return PKV_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks, const void* src_k, const void* src_v,
+                           int src_num_blocks, const pkv_cache_desc* layout, const int32_t* block_pairs,
+                           int num_pairs, pkv_stream_t stream) {
+  using namespace pkv;
+  pkv_status st = check_cache_desc(layout);
+  if (st != PKV_OK) return st;
+  if (num_pairs < 0 || dst_num_blocks <= 0 || src_num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!dst_k || !dst_v || !src_k || !src_v || !block_pairs) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(dst_k) || !aligned16(dst_v) || !aligned16(src_k) || !aligned16(src_v) ||
+      (reinterpret_cast<uintptr_t>(block_pairs) & 7u))
+    return PKV_ERR_INVALID_ARG;
+  if (num_pairs > 65535) return PKV_ERR_UNSUPPORTED;
+  unsigned* err = error_word_ptr();
+  if (!err) return PKV_ERR_CUDA;
+  const int64_t block_bytes =
+      int64_t(layout->num_kv_heads) * layout->block_size * layout->head_dim * dtype_bytes(layout->kv_dtype);
+  if (launch_pdl(swap_blocks_kernel, dim3(num_pairs, 2), dim3(kThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+                 static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v), static_cast<const uint4*>(src_k),
+                 static_cast<const uint4*>(src_v), block_pairs, num_pairs, src_num_blocks, dst_num_blocks,
+                 block_bytes / 16, err) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 }  // extern "C"

@@ -57,6 +57,11 @@ def test_argument_checks_run_on_host_without_gpu():
     assert L.pkv_kv_write(16, 16, 1, 0, 16, 16, 16, ctypes.byref(desc), None) == 0
     assert L.pkv_copy_blocks(16, 16, ctypes.byref(desc), 16, 0, None) == 0
     assert L.pkv_decode_workspace_bytes(4, 6, 4, 128, 16, 100, 0) == 0       # bad split -> 0
+    # swap_blocks: misaligned host pool, empty destination pool, missing pairs; no pairs is fine
+    assert L.pkv_swap_blocks(16, 16, 8, 24, 16, 8, ctypes.byref(desc), 16, 2, None) == 1
+    assert L.pkv_swap_blocks(16, 16, 0, 16, 16, 8, ctypes.byref(desc), 16, 2, None) == 1
+    assert L.pkv_swap_blocks(16, 16, 8, 16, 16, 8, ctypes.byref(desc), None, 2, None) == 1
+    assert L.pkv_swap_blocks(16, 16, 8, 16, 16, 8, ctypes.byref(desc), 16, 0, None) == 0
 
 
 # ---------------------------------------------------------------------------------------
@@ -112,6 +117,9 @@ def _random_ops(seed, n_ops=3000, nb=300, bs=16):
     live, nxt = [], 0
     for _ in range(n_ops):
         r = rng.random()
+        if live and r > 0.93:                   # preemption by swapping, and the way back
+            ops.append(("swap_out" if r < 0.965 else "swap_in", int(rng.choice(live))))
+            continue
         if r < 0.2 or not live:
             ops.append(("allocate", nxt, int(rng.integers(0, 120)))); live.append(nxt); nxt += 1
         elif r < 0.55:
@@ -132,13 +140,15 @@ def _random_ops(seed, n_ops=3000, nb=300, bs=16):
 def test_block_manager_matches_oracle_model(seed):
     from oracle.block_manager import BlockManagerModel, NoBlocks
     from paged_kv_cache_160_gb300 import BlockManager, NoBlocksError
-    nb, bs, mb = 300, 16, 64
+    nb, bs, mb, nh = 300, 16, 64, 200
     model, prod = BlockManagerModel(nb, bs), BlockManager(nb, bs)
+    model.set_host_pool(nh)
+    prod.set_host_pool(nh)
     live = set()
     for op in _random_ops(seed, nb=nb, bs=bs):
         kind = op[0]
         if kind == "step_decode":
-            seqs = [s for s in op[1] if s in live]
+            seqs = [s for s in op[1] if s in live and not model.swapped.get(s)]
             if not seqs:
                 continue
             # the model has no batch call: all-or-nothing on the number of blocks needed
@@ -157,7 +167,11 @@ def test_block_manager_matches_oracle_model(seed):
             tables, lens = model.export(seqs, mb)
             assert got == (slots, cows, tables, lens)
             continue
-        if kind in ("append_slot", "append_slots", "free", "fork") and op[1] not in live:
+        if kind in ("append_slot", "append_slots", "free", "fork", "swap_out", "swap_in") and op[1] not in live:
+            continue
+        if kind in ("append_slot", "append_slots", "fork", "swap_out") and model.swapped.get(op[1]):
+            continue
+        if kind == "swap_in" and not model.swapped.get(op[1]):
             continue
         res = {}
         for name, side in (("m", model), ("p", prod)):
@@ -172,6 +186,10 @@ def test_block_manager_matches_oracle_model(seed):
                     side.fork(op[1], op[2]); res[name] = "ok"
                 elif kind == "free":
                     side.free(op[1]); res[name] = "ok"
+                elif kind == "swap_out":
+                    res[name] = side.swap_out(op[1])
+                elif kind == "swap_in":
+                    res[name] = side.swap_in(op[1])
             except (NoBlocks, NoBlocksError):
                 res[name] = "noblocks"
         assert res["m"] == res["p"], op
@@ -183,10 +201,41 @@ def test_block_manager_matches_oracle_model(seed):
             elif kind == "free":
                 live.discard(op[1])
         assert prod.num_free() == model.num_free()
+        assert prod.num_free_host() == len(model.host_free)
     assert prod.free_queue() == list(model.free_queue)
+    assert all(prod.is_swapped(s) == int(bool(model.swapped.get(s))) for s in live)
     assert [prod.ref_cnt(b) for b in range(nb)] == model.ref_cnt
-    seqs = sorted(live)
+    seqs = sorted(s for s in live if not model.swapped.get(s))
     assert prod.export(seqs, mb) == model.export(seqs, mb)
+
+
+def test_swap_out_and_in_follow_the_preemption_steps():
+    """Lecture 33 §5.2: the victim's blocks go to host memory, its device blocks return to
+    the pool for others, and later it comes back into fresh device blocks."""
+    from paged_kv_cache_160_gb300 import BlockManager, NoBlocksError, PkvError
+    bm = BlockManager(8, 4)
+    bm.set_host_pool(3)
+    bm.allocate(0, 10)                           # blocks 0, 1, 2
+    bm.allocate(1, 4)                            # block 3
+    bm.fork(1, 2)                                # block 3 shared by 1 and 2
+    assert bm.swap_out(0) == [(0, 0), (1, 1), (2, 2)]
+    assert bm.free_queue() == [4, 5, 6, 7, 0, 1, 2] and bm.num_free_host() == 0
+    with pytest.raises(PkvError):                # a swapped sequence neither appends nor exports
+        bm.append_slot(0)
+    with pytest.raises(PkvError):
+        bm.export([0], 4)
+    with pytest.raises(NoBlocksError):           # the host pool is full
+        bm.swap_out(1)
+    bm.allocate(3, 16)                           # reuses 4, 5, 6, 7
+    with pytest.raises(NoBlocksError):           # needs 4 device blocks, only 0, 1, 2 are free
+        bm.allocate(4, 13)
+    assert bm.swap_in(0) == [(0, 0), (1, 1), (2, 2)]
+    assert bm.export([0], 4) == ([[0, 1, 2, -1]], [10]) and bm.num_free_host() == 3
+    bm.free(3)
+    assert bm.swap_out(2) == [(3, 0)]            # shared block: stays for sequence 1, copied for 2
+    assert bm.ref_cnt(3) == 1
+    assert bm.swap_in(2) == [(0, 4)]
+    assert bm.export([1, 2], 2) == ([[3, -1], [4, -1]], [4, 4])
 
 
 def test_synthetic_plans_agree_on_both_sides():
