@@ -293,6 +293,26 @@ PKV_API pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq);
 PKV_API pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n, int max_blocks,
                          int32_t* tables, int32_t* lens);
 
+/* Prefix caching ("PagedAttention: manage the KV cache like virtual memory" §3.4–§3.5;
+ * Lecture 33 §6.2–§6.3).  A full block is named by h_i = FNV-1a-64(h_{i-1} as 8 bytes
+ * little-endian, then its block_size token ids as 4 bytes little-endian each), with h_{-1} =
+ * the FNV offset basis 0xcbf29ce484222325, so equal hashes mean equal prefixes.  Admission of
+ * a prompt matches its full blocks in order against the cached hashes and stops at the first
+ * miss; each hit is "touched" (ref_cnt + 1, and a block nobody held is unlinked from the
+ * middle of the free queue in O(1)).  The remaining blocks are popped from the free queue's
+ * head, and the new full blocks are registered under their hashes.  *n_cached_tokens = hits x
+ * block_size: those tokens' K/V are already in the pool and need no prefill; the others'
+ * K/V become valid once the caller's prefill for this sequence has run.  Freed blocks keep
+ * their hash (cached and free) until popped for new contents, which drops the hash.  Blocks
+ * that fill up during decode are not registered (the manager does not see token ids there).
+ * PKV_ERR_NO_BLOCKS, changing nothing, if the misses need more blocks than are free once the
+ * hit blocks leave the queue. */
+PKV_API pkv_status pkv_bm_allocate_cached(pkv_block_manager* bm, int64_t seq, const int32_t* tokens, int n_tokens,
+                                          int* n_cached_tokens);
+/* 1 and *hash = the block's registered hash; 0 if it has none; -1 on bad arguments. */
+PKV_API int pkv_bm_block_hash(const pkv_block_manager* bm, int block, uint64_t* hash);
+PKV_API int pkv_bm_num_cached(const pkv_block_manager* bm);   /* registered hashes */
+
 /* Preemption by swapping ("Lecture 33 — KV Cache management" §5.2).  The host pool is a
  * second set of num_host_blocks blocks (ids 0..num_host_blocks-1 of a caller-owned pinned
  * buffer with the device pool's block layout) with its own FIFO free queue.  Resizing is

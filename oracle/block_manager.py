@@ -29,11 +29,48 @@ Readings where the pages are silent:
   sequence stays for it; the swapped sequence takes its own host copy).  Swap-in pops
   one device block per table entry in order and returns the host blocks to the host
   queue's tail in table order.  A swapped sequence can only be freed or swapped in.
+
+Prefix caching ("PagedAttention: manage the KV cache like virtual memory" §3.4–§3.5;
+"Lecture 33" §6.2–§6.3): a full block is named by its parent's name and its tokens, so a
+name stands for the whole token prefix up to the block's end.  The model keys blocks by that
+exact prefix (a tuple of token ids), so it never confuses two prefixes; ``block_hash``
+computes the 64-bit FNV-1a chain the library publishes for the same key.  Admission matches
+the prompt's full blocks in order and stops at the first miss; a hit raises the block's count
+and takes it out of the free queue if nobody held it; the other blocks are popped and the new
+full ones registered.  A popped block loses its registration (new contents).  Readings: the
+first block's parent name is the FNV offset basis; blocks filled during decode are not
+registered (token ids are not known there).
 """
 from __future__ import annotations
 
 from collections import deque
 from typing import Dict, List, Optional, Sequence, Tuple
+
+FNV64_OFFSET = 0xCBF29CE484222325
+FNV64_PRIME = 0x100000001B3
+
+
+def fnv1a64(data: bytes, h: int = FNV64_OFFSET) -> int:
+    """64-bit FNV-1a: for each byte, xor it in, then multiply by the FNV prime (mod 2^64)."""
+    for byte in data:
+        h ^= byte
+        h = (h * FNV64_PRIME) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def block_hash(parent: int, tokens: Sequence[int]) -> int:
+    """Name of a full block: FNV-1a over the parent's name (8 bytes little-endian) then the
+    token ids (4 bytes little-endian each)."""
+    data = parent.to_bytes(8, "little") + b"".join((int(t) & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens)
+    return fnv1a64(data)
+
+
+def prefix_hash(prefix: Sequence[int], block_size: int) -> int:
+    """Name of the last full block of ``prefix`` (len a multiple of block_size)."""
+    h = FNV64_OFFSET
+    for i in range(0, len(prefix), block_size):
+        h = block_hash(h, prefix[i:i + block_size])
+    return h
 
 
 class BlockManagerError(Exception):
@@ -58,6 +95,8 @@ class BlockManagerModel:
         self.num_tokens: Dict[int, int] = {}
         self.host_free: deque = deque()
         self.swapped: Dict[int, bool] = {}
+        self.cached: Dict[tuple, int] = {}         # token prefix -> block holding its last full block
+        self.block_key: Dict[int, tuple] = {}      # registered block -> its prefix
 
     # -- pool ---------------------------------------------------------------------------
     def num_free(self) -> int:
@@ -69,6 +108,9 @@ class BlockManagerModel:
         b = self.free_queue.popleft()
         assert self.ref_cnt[b] == 0
         self.ref_cnt[b] = 1
+        key = self.block_key.pop(b, None)          # new contents: the cached prefix is gone
+        if key is not None and self.cached.get(key) == b:
+            del self.cached[key]
         return b
 
     def _release(self, b: int) -> None:
@@ -107,6 +149,44 @@ class BlockManagerModel:
         if seq not in self.tables or self.swapped.get(seq):
             raise InvalidArg("not a resident sequence")
         return self.tables[seq]
+
+    def allocate_cached(self, seq: int, tokens: Sequence[int]) -> int:
+        """Admit a prompt, re-using the blocks of its longest cached full-block prefix;
+        returns the number of cached tokens."""
+        if seq in self.tables:
+            raise InvalidArg("sequence exists")
+        bs = self.block_size
+        tokens = [int(t) for t in tokens]
+        n_full, need = len(tokens) // bs, -(-len(tokens) // bs)
+        keys = [tuple(tokens[:(i + 1) * bs]) for i in range(n_full)]
+        hits = []
+        for k in keys:
+            b = self.cached.get(k)
+            if b is None:
+                break
+            hits.append(b)
+        held_free = sum(1 for b in hits if self.ref_cnt[b] == 0)
+        if need - len(hits) > len(self.free_queue) - held_free:
+            raise NoBlocks("not enough free blocks")
+        table = []
+        for b in hits:
+            if self.ref_cnt[b] == 0:
+                self.free_queue.remove(b)
+            self.ref_cnt[b] += 1
+            table.append(b)
+        for i in range(len(hits), need):
+            b = self._pop()
+            table.append(b)
+            if i < n_full and keys[i] not in self.cached:
+                self.cached[keys[i]] = b
+                self.block_key[b] = keys[i]
+        self.tables[seq] = table
+        self.num_tokens[seq] = len(tokens)
+        return len(hits) * bs
+
+    def block_hash(self, block: int) -> Optional[int]:
+        key = self.block_key.get(block)
+        return None if key is None else prefix_hash(key, self.block_size)
 
     def append_slot(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
         """Reserve the slot of the sequence's next token; returns (slot, cow_pair or None)."""

@@ -95,6 +95,12 @@ def _load() -> ctypes.CDLL:
     lib.pkv_bm_free.argtypes = [BM, c_int64]
     lib.pkv_bm_export.restype = S
     lib.pkv_bm_export.argtypes = [BM, POINTER(c_int64), c_int, c_int, POINTER(c_int32), POINTER(c_int32)]
+    lib.pkv_bm_allocate_cached.restype = S
+    lib.pkv_bm_allocate_cached.argtypes = [BM, c_int64, POINTER(c_int32), c_int, POINTER(c_int)]
+    lib.pkv_bm_block_hash.restype = c_int
+    lib.pkv_bm_block_hash.argtypes = [BM, c_int, POINTER(ctypes.c_uint64)]
+    lib.pkv_bm_num_cached.restype = c_int
+    lib.pkv_bm_num_cached.argtypes = [BM]
     lib.pkv_bm_set_host_pool.restype = S
     lib.pkv_bm_set_host_pool.argtypes = [BM, c_int]
     lib.pkv_bm_swap_out.restype = S
@@ -322,6 +328,23 @@ class BlockManager:
 
     def free(self, seq: int) -> None:
         _check(lib.pkv_bm_free(self._h, seq), "pkv_bm_free")
+
+    def allocate_cached(self, seq: int, tokens: Sequence[int]) -> int:
+        """Admit a prompt reusing its cached full-block prefix; returns the cached token count."""
+        n = c_int()
+        _check(lib.pkv_bm_allocate_cached(self._h, seq, _i32(tokens), len(tokens), ctypes.byref(n)),
+               "pkv_bm_allocate_cached")
+        return n.value
+
+    def block_hash(self, block: int) -> Optional[int]:
+        h = ctypes.c_uint64()
+        r = lib.pkv_bm_block_hash(self._h, block, ctypes.byref(h))
+        if r < 0:
+            raise PkvError(1, "pkv_bm_block_hash: bad arguments")
+        return h.value if r == 1 else None
+
+    def num_cached(self) -> int:
+        return lib.pkv_bm_num_cached(self._h)
 
     def set_host_pool(self, num_host_blocks: int) -> None:
         _check(lib.pkv_bm_set_host_pool(self._h, num_host_blocks), "pkv_bm_set_host_pool")

@@ -1,7 +1,11 @@
 // Host block manager: the free-block queue, per-block ref_cnt and per-sequence block
 // tables of "PagedAttention: manage the KV cache like virtual memory" §3.2–§3.3, with
 // fork and copy-on-write from "Lecture 33 — KV Cache management" §2.4 and preemption by
-// swapping (a host-memory block pool with its own FIFO queue) from its §5.2.
+// swapping (a host-memory block pool with its own FIFO queue) from its §5.2, and prefix
+// caching from "PagedAttention: manage the KV cache like virtual memory" §3.4–§3.5: a full
+// block is named by a hash of its parent block's hash and its tokens; a hit re-uses the block
+// (taking it out of the middle of the free queue if nobody held it), and a cached block that
+// nobody holds stays reusable until it is popped for new data.
 //
 // The free queue is an intrusive doubly linked list over block ids (allocate pops the
 // head, free pushes the tail, a claimed block is unlinked from the middle in O(1)).
@@ -35,6 +39,9 @@ struct pkv_block_manager {
   int32_t head = -1, tail = -1;
   int num_free = 0;
   std::unordered_map<int64_t, Seq> seqs;
+  std::vector<uint64_t> bhash;       // prefix-cache hash of a full block ...
+  std::vector<uint8_t> has_hash;     // ... valid when set
+  std::unordered_map<uint64_t, int32_t> hash_to_block;
   std::deque<int32_t> host_free;     // host swap pool: FIFO of free host block ids
   int num_host_blocks = 0;
   int num_swapped = 0;
@@ -64,7 +71,17 @@ struct pkv_block_manager {
     int32_t b = head;
     unlink(b);
     ref[b] = 1;
+    if (has_hash[b]) {    // the block gets new contents: its cached prefix is gone
+      auto it = hash_to_block.find(bhash[b]);
+      if (it != hash_to_block.end() && it->second == b) hash_to_block.erase(it);
+      has_hash[b] = 0;
+    }
     return b;
+  }
+  // Prefix-cache hit: one more holder; a block nobody held leaves the free queue.
+  void touch(int32_t b) {
+    if (in_free[b]) unlink(b);
+    ++ref[b];
   }
   void release(int32_t b) {
     if (--ref[b] == 0) push_tail(b);
@@ -117,6 +134,8 @@ pkv_status pkv_bm_create(int num_blocks, int block_size, pkv_block_manager** out
   bm->prev.assign(num_blocks, -1);
   bm->next.assign(num_blocks, -1);
   bm->in_free.assign(num_blocks, 0);
+  bm->bhash.assign(num_blocks, 0);
+  bm->has_hash.assign(num_blocks, 0);
   for (int b = 0; b < num_blocks; ++b) bm->push_tail(b);
   *out = bm;
   return PKV_OK;
@@ -272,6 +291,76 @@ pkv_status pkv_bm_export(const pkv_block_manager* bm, const int64_t* seqs, int n
   }
   return PKV_OK;
 }
+
+// 64-bit FNV-1a over the parent hash (8 bytes, little-endian) then the block's token ids
+// (4 bytes each, little-endian); the first block's parent hash is the FNV offset basis.
+static uint64_t fnv1a_block(uint64_t parent, const int32_t* tokens, int n) {
+  uint64_t h = 0xcbf29ce484222325ull;
+  auto mix = [&](uint8_t byte) {
+    h ^= byte;
+    h *= 0x100000001b3ull;
+  };
+  for (int i = 0; i < 8; ++i) mix(uint8_t(parent >> (8 * i)));
+  for (int t = 0; t < n; ++t) {
+    const uint32_t u = uint32_t(tokens[t]);
+    for (int i = 0; i < 4; ++i) mix(uint8_t(u >> (8 * i)));
+  }
+  return h;
+}
+
+pkv_status pkv_bm_allocate_cached(pkv_block_manager* bm, int64_t seq, const int32_t* tokens, int n_tokens,
+                                  int* n_cached_tokens) {
+  if (!bm || n_tokens < 0 || (n_tokens > 0 && !tokens) || !n_cached_tokens || bm->seqs.count(seq))
+    return PKV_ERR_INVALID_ARG;
+  const int bs = bm->block_size;
+  const int n_full = n_tokens / bs;
+  const int64_t need_total = bm->blocks_for(n_tokens);
+  // Longest run of cached full blocks from the start (the hash chain makes it a prefix).
+  std::vector<uint64_t> hashes(n_full);
+  std::vector<int32_t> hits;
+  uint64_t parent = 0xcbf29ce484222325ull;
+  int held_free = 0;                         // hits now in the free queue (they leave it)
+  for (int i = 0; i < n_full; ++i) {
+    hashes[i] = fnv1a_block(parent, tokens + int64_t(i) * bs, bs);
+    parent = hashes[i];
+    if (int(hits.size()) == i) {
+      auto it = bm->hash_to_block.find(hashes[i]);
+      if (it != bm->hash_to_block.end()) {
+        hits.push_back(it->second);
+        if (bm->ref[it->second] == 0) ++held_free;
+      }
+    }
+  }
+  const int64_t misses = need_total - int64_t(hits.size());
+  if (misses > bm->num_free - held_free) return PKV_ERR_NO_BLOCKS;
+  Seq s;
+  s.n_tokens = n_tokens;
+  for (int32_t b : hits) {
+    bm->touch(b);
+    s.blocks.push_back(b);
+  }
+  for (int64_t i = int64_t(hits.size()); i < need_total; ++i) {
+    const int32_t b = bm->pop_head();
+    s.blocks.push_back(b);
+    if (i < n_full && !bm->hash_to_block.count(hashes[i])) {   // register the new full block
+      bm->bhash[b] = hashes[i];
+      bm->has_hash[b] = 1;
+      bm->hash_to_block.emplace(hashes[i], b);
+    }
+  }
+  *n_cached_tokens = int(hits.size()) * bs;
+  bm->seqs.emplace(seq, std::move(s));
+  return PKV_OK;
+}
+
+int pkv_bm_block_hash(const pkv_block_manager* bm, int block, uint64_t* hash) {
+  if (!bm || block < 0 || block >= bm->num_blocks || !hash) return -1;
+  if (!bm->has_hash[block]) return 0;
+  *hash = bm->bhash[block];
+  return 1;
+}
+
+int pkv_bm_num_cached(const pkv_block_manager* bm) { return bm ? int(bm->hash_to_block.size()) : -1; }
 
 pkv_status pkv_bm_set_host_pool(pkv_block_manager* bm, int num_host_blocks) {
   if (!bm || num_host_blocks < 0 || bm->num_swapped > 0) return PKV_ERR_INVALID_ARG;
