@@ -76,7 +76,7 @@ enum {
 typedef struct {
   int num_blocks;            /* physical blocks in the pool */
   int num_kv_heads;
-  int block_size;            /* tokens per block; 16 */
+  int block_size;            /* tokens per block: 16, or 32 (the attention kernels read it as two 16-row tiles) */
   int head_dim;              /* 64 or 128 */
   pkv_dtype kv_dtype;
   const float* k_scale;      /* (device) [num_kv_heads] fp32, e4m3 caches only, else NULL */
@@ -166,10 +166,10 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_k
  *                  written this step
  *   max_context_len host upper bound of context_lens; larger lengths are clamped to it
  *                  (and to max_blocks_per_seq * block_size) and flagged PKV_DEVERR_CONTEXT_LEN
- *   partition_size  0 = balanced split; else split granularity in tokens (multiple of block_size)
+ *   partition_size  0 = balanced split; else split granularity in tokens (multiple of 16)
  *   workspace       (device) >= pkv_decode_workspace_bytes(...) bytes
  * Supported: kv f16/bf16 with the same q dtype, or e4m3 kv with f16/bf16 q (the e4m3
- * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16;
+ * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16 or 32;
  * num_heads / num_kv_heads in 1..8.
  * Launch order: the decode kernel is launched as a programmatic dependent of the previous
  * kernel on `stream`.  If that kernel allows early dependent launch (pkv_kv_write does), the
@@ -222,7 +222,7 @@ PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype 
  *   q_start_pos   (device) int32 [num_chunks]
  *   block_tables  (device) int32 [num_chunks][max_blocks_per_seq]
  *   max_q_len     host upper bound of the chunks' lengths (sizes the grid)
- * Supported: f16/bf16 cache with the same q dtype, head_dim 128, block_size 16,
+ * Supported: f16/bf16 cache with the same q dtype, head_dim 128, block_size 16 or 32,
  * num_heads / num_kv_heads in 1..8.  Tensor cores (tcgen05, TMEM accumulators), K/V
  * tiles fetched by TMA straight from the physical blocks.
  */

@@ -41,7 +41,7 @@ namespace {
 
 enum { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
 
-constexpr int kBS = 16;        // tokens per block
+constexpr int kBS = 16;        // tokens per tile: a 16-token block, or half of a 32-token one
 constexpr int kMaxWarps = 12;  // worker warps per CTA (3 per SM sub-partition)
 constexpr int kMaxGroup = 8;   // query heads per kv head handled by one n=8 MMA tile
 
@@ -70,9 +70,11 @@ struct DecodeParams {
   int num_kv_heads;
   int group;
   int max_blocks;
-  int max_len;            // min(max_blocks * 16, max_context_len): lengths are clamped to it
+  int max_len;            // min(max_blocks * block_size, max_context_len): lengths are clamped to it
   int num_blocks;
-  int part_blocks;        // blocks per partition; 0 = balanced split
+  int block_size;         // tokens per pool block: 16 or 32 (1 or 2 tiles)
+  int tile_shift;         // log2(block_size / 16)
+  int part_blocks;        // tiles per partition; 0 = balanced split
   int num_workers;        // gridDim.x * worker warps per CTA
   float scale_log2;       // softmax scale * log2(e)
   int4* seg_desc;         // [num_seqs * num_kv_heads]: (first worker, pieces, first worker's slot parity, 0)
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int64_t t = t_begin + int64_t(win) * 32 + lane;
     if (t >= t_end) return -1;
     const Tile c = locate(t);
-    return p.block_tables[int64_t(c.s) * p.max_blocks + c.b];
+    return p.block_tables[int64_t(c.s) * p.max_blocks + (c.b >> p.tile_shift)];
   };
   int bid_cur = load_window(0);                // in flight while the piece count below is worked out
   int bid_nxt = n > 32 ? load_window(1) : -1;
@@ -306,7 +308,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     valid |= 1u << st;
     mbar_arrive_expect_tx(bar, C::kStageBytes);
-    const int y = int((int64_t(pb) * Hkv + c.h) * kBS);
+    // First pool row of the tile: the (block, kv head) rows start at (pb * Hkv + h) * block_size
+    // and a 32-token block holds the tile's 16 rows at offset 0 or 16.
+    const int y = int((int64_t(pb) * Hkv + c.h) * p.block_size + (c.b & ((1 << p.tile_shift) - 1)) * kBS);
     uint8_t* kdst = my_stages + st * C::kStageBytes;
     if constexpr (C::kNBox == 2) {
       // One 3-D box brings both 128-byte halves of the 16 rows: [half 0: 16 x 128 B][half 1].
@@ -751,8 +755,8 @@ extern "C" {
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                                   int max_context_len, int partition_size) {
   using namespace pkv;
-  if (num_seqs <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || block_size != kBS || partition_size < 0 ||
-      partition_size % kBS)
+  if (num_seqs <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || (block_size != 16 && block_size != 32) ||
+      partition_size < 0 || partition_size % kBS)
     return 0;
   const int group = num_heads / num_kv_heads;
   const int workers = decode_grid() * kMaxWarps;
@@ -779,13 +783,14 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   if (partition_size % kBS) return PKV_ERR_INVALID_ARG;
   if (max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
   const int group = num_heads / cache->num_kv_heads;
-  if (cache->block_size != kBS || group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
+  if ((cache->block_size != 16 && cache->block_size != 32) || group > kMaxGroup) return PKV_ERR_UNSUPPORTED;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   const int D = cache->head_dim;
   if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
   if (cache->kv_dtype != PKV_FP8_E4M3 && cache->kv_dtype != q_dtype) return PKV_ERR_UNSUPPORTED;
   if (cache->kv_dtype == PKV_FP8_E4M3 && D != 128) return PKV_ERR_UNSUPPORTED;
-  if (int64_t(cache->num_blocks) * cache->num_kv_heads * kBS >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  if (int64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size >= (int64_t(1) << 31))
+    return PKV_ERR_UNSUPPORTED;
 
   const int grid = decode_grid();
   const int part_blocks = partition_size / kBS;
@@ -795,13 +800,13 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
 
-  // Tensor maps: the pool as rows of head_dim elements; a box is one (block, kv head) tile of
-  // 16 rows.  Rows of 128 bytes are one 2-D box; rows of 256 bytes (2-byte, head_dim 128) are
+  // Tensor maps: the pool as rows of head_dim elements; a box is one 16-row tile of a (block,
+  // kv head).  Rows of 128 bytes are one 2-D box; rows of 256 bytes (2-byte, head_dim 128) are
   // viewed as (64 elements, rows, 2 halves) so one 3-D box lands as two swizzled halves.
   CUtensorMap tk, tv;
   const bool fp8 = cache->kv_dtype == PKV_FP8_E4M3;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * kBS;
+  const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size;
   const uint64_t row_bytes = uint64_t(D) * dtype_bytes(cache->kv_dtype);
   bool enc;
   if (row_bytes == 256) {
@@ -825,8 +830,10 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   prm.num_kv_heads = cache->num_kv_heads;
   prm.group = group;
   prm.max_blocks = max_blocks_per_seq;
-  prm.max_len = int(std::min<int64_t>(int64_t(max_blocks_per_seq) * kBS, max_context_len));
+  prm.max_len = int(std::min<int64_t>(int64_t(max_blocks_per_seq) * cache->block_size, max_context_len));
   prm.num_blocks = cache->num_blocks;
+  prm.block_size = cache->block_size;
+  prm.tile_shift = cache->block_size == 32 ? 1 : 0;
   prm.part_blocks = part_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.seg_desc = reinterpret_cast<int4*>(ws + lay.desc);

@@ -35,7 +35,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kBS = 16;
+constexpr int kBS = 16;        // rows per TMA box: a 16-token block, or half of a 32-token one
 constexpr int kD = 128;
 constexpr int kTile = 128;                    // query rows per CTA and keys per iteration
 constexpr int kThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
@@ -61,6 +61,8 @@ struct PrefillParams {
   const int32_t* block_tables;
   int max_blocks;
   int num_blocks;
+  int block_size;         // tokens per pool block: 16 or 32
+  int tile_shift;         // log2(block_size / 16)
   int num_heads;
   int num_kv_heads;
   float scale_log2;
@@ -90,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (qlen <= 0 || r0 >= qlen) return;                       // no rows for this CTA
   const int start = p.q_start_pos[c];
   const int ctx = start + qlen;                              // keys 0 .. ctx-1 exist
-  if (start < 0 || ctx > p.max_blocks * kBS) {
+  if (start < 0 || ctx > p.max_blocks * p.block_size) {
     if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
     return;
   }
@@ -154,19 +156,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sQ, &tmq, &bar_q, 0, hq, q0 + r0, pol_q);
       tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq, q0 + r0, pol_q);
     }
-    // Pool rows of the sequence's logical blocks, 32 per window (4 tiles): lane i holds block
-    // 32 * w + i.  Blocks past the sequence map to block 0 (their rows are masked / zeroed).
+    // Pool rows of the sequence's 16-row units, 32 per window (4 tiles): lane i holds unit
+    // 32 * w + i, which is block unit >> tile_shift at row offset 16 * (unit & mask).  Units
+    // past the sequence map to block 0 (their rows are masked / zeroed).
     auto load_window = [&](int w) -> int {
       const int lb = 32 * w + lane;
       int pb = 0;
       if (lb < nb) {
-        pb = table[lb];
+        pb = table[lb >> p.tile_shift];
         if (pb < 0 || pb >= p.num_blocks) {
           set_error(p.err, PKV_DEVERR_BLOCK_ID);
           pb = 0;
         }
       }
-      return (pb * p.num_kv_heads + h) * kBS;
+      return (pb * p.num_kv_heads + h) * p.block_size + (lb & ((1 << p.tile_shift) - 1)) * kBS;
     };
     struct Window {
       int cur, nxt, w;
@@ -468,18 +471,20 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
     return PKV_ERR_INVALID_ARG;
   if (num_heads % cache->num_kv_heads || max_blocks_per_seq == 0) return PKV_ERR_INVALID_ARG;
   if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-  if (cache->kv_dtype != q_dtype || cache->head_dim != kD || cache->block_size != kBS) return PKV_ERR_UNSUPPORTED;
+  if (cache->kv_dtype != q_dtype || cache->head_dim != kD || (cache->block_size != 16 && cache->block_size != 32))
+    return PKV_ERR_UNSUPPORTED;
   if (num_chunks > 65535 || num_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (!(scale > 0.f)) return PKV_ERR_INVALID_ARG;          // the softmax takes max(s) * scale
-  if (int64_t(cache->num_blocks) * cache->num_kv_heads * kBS >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  if (int64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size >= (int64_t(1) << 31))
+    return PKV_ERR_UNSUPPORTED;
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
 
   CUtensorMap tq, tk, tv;
-  const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * kBS;
+  const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size;
   if (!encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, q, kD, uint64_t(num_heads), uint64_t(total_q), kD * 2,
                       uint64_t(num_heads) * kD * 2, 64, 1, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      // K / V as (64 dims, rows, 2 halves): one box = a block's 16 rows of both halves
+      // K / V as (64 dims, rows, 2 halves): one box = 16 rows of a block, both halves
       !encode_tmap_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, k_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 2,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, v_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 2,
@@ -493,6 +498,8 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   prm.block_tables = block_tables;
   prm.max_blocks = max_blocks_per_seq;
   prm.num_blocks = cache->num_blocks;
+  prm.block_size = cache->block_size;
+  prm.tile_shift = cache->block_size == 32 ? 1 : 0;
   prm.num_heads = num_heads;
   prm.num_kv_heads = cache->num_kv_heads;
   prm.scale_log2 = scale * 1.4426950408889634f;

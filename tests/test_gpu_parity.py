@@ -126,6 +126,22 @@ def test_very_large_batch_takes_the_four_warp_layout():
     _check_case(case, decode_rows=rows, compare_caches=False)
 
 
+BS32 = [
+    # 32-token blocks: each is two 16-row tiles.  Lengths straddle tile and block edges;
+    # a 48-token partition ends inside a block.
+    ("bs32_gqa7_bf16", [1, 16, 17, 31, 32, 33, 100, 700], 28, 4, 128, "bf16", "bf16", 0),
+    ("bs32_e4m3_part512", [5, 511, 512, 513, 1500], 32, 8, 128, "bf16", "e4m3", 512),
+    ("bs32_f16_d64_part48", [3, 47, 48, 49, 250], 8, 2, 64, "f16", "f16", 48),
+]
+
+
+@pytest.mark.parametrize("name,lens,hq,hkv,d,qd,kd,part", BS32, ids=[s[0] for s in BS32])
+def test_block_size_32(name, lens, hq, hkv, d, qd, kd, part):
+    case = synth.make_decode_case(name, 83, lens, hq, hkv, d, qd, kd, block_size=32, partition_size=part,
+                                  unused_fill="nan")
+    _check_case(case)
+
+
 @pytest.mark.parametrize("kd", ["bf16", "e4m3"])
 def test_unused_slots_hold_nan(kd):
     """Rows past each sequence's end hold NaN; they must never reach the output."""

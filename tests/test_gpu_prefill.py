@@ -97,6 +97,11 @@ def test_varlen_chunks_ragged(dtype):
     _check(_case(2, [(37, 200), (0, 5), (300, 129), (1000, 1), (128, 256)], 8, 2, dtype))
 
 
+def test_block_size_32_chunks():
+    """32-token blocks: the kernel gathers each 128-key tile as eight 16-row halves of blocks."""
+    _check(_case(5, [(37, 200), (0, 5), (300, 129), (1000, 1)], 8, 2, "bf16", nan_fill=True, bs=32))
+
+
 def test_gqa7_long_prefix():
     _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
 
