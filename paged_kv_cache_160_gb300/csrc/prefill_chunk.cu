@@ -8,14 +8,16 @@
 //
 // GB300 design (one CTA per 128 query rows of one query head, 1 CTA per SM):
 //   warp 0             : TMA producer — Q once (128 rows x 128 dims), then per 128-key tile
-//                        the 8 physical blocks of K and of V (16-row boxes gathered by block
-//                        id; the block table is read 32 entries at a time, lane-parallel, one
-//                        window ahead; one 3-D TMA box per block brings both 128-byte halves
-//                        of its 16 rows); K and V (3 stages each) run ahead, each stage
-//                        refilled as soon as its MMA is done.
+//                        the 8 physical 16-row blocks of K and of V, gathered by block id
+//                        (the block table is read 32 entries at a time, lane-parallel, one
+//                        window ahead).  K lands as [64-dim half][block][16 rows] (two 2-D
+//                        boxes per block), so its 8-row groups are evenly spaced and one
+//                        N = 128 MMA covers the tile; V lands as [block][half][16 rows] (one
+//                        3-D box per block).  K and V (3 stages each) run ahead, each stage
+//                        refilled once every CTA of the cluster has released it.
 //   warp 1             : owns 512 TMEM columns; one thread issues tcgen05.mma —
-//                        S_j = Q K_j^T (M = 128, two N = 64 halves, K = 128, both operands
-//                        K-major in smem) into one of three TMEM S buffers, and
+//                        S_j = Q K_j^T (M = N = 128, K = 128, both operands K-major in smem,
+//                        column n of S = key n of the tile) into one of three TMEM S buffers, and
 //                        O += P_j V_j into the TMEM O accumulator, with P read from TMEM (it
 //                        overwrites S_j in place) and V from shared memory as an MN-major
 //                        operand.  S of later tiles overlaps the softmax of earlier ones, and
@@ -42,8 +44,10 @@ constexpr int kThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2
 constexpr uint32_t kTmemCols = 512;           // S0 | S1 | S2 | O, 128 columns each
 constexpr int kHalfBytes = kTile * 128;       // [128 rows][64 elements] of 2 bytes = 16 KB
 constexpr int kTileBytes = 2 * kHalfBytes;    // one 128 x 128 operand = 32 KB
-// K and V tiles hold 8 blocks of 4 KB: block b at 4 KB * b = [dims 0..63: 16 rows x 128 B]
-// [dims 64..127: 16 rows x 128 B], each half 128-byte swizzled (one TMA box per block).
+// A V tile holds 8 blocks of 4 KB: block b at 4 KB * b = [dims 0..63: 16 rows x 128 B]
+// [dims 64..127: 16 rows x 128 B], each half 128-byte swizzled (one 3-D TMA box per block).
+// A K tile holds the same bytes as [dims 0..63: block 0..7 x 16 rows][dims 64..127: ...]
+// (two 2-D boxes of 2 KB per block).
 constexpr int kBlockBytes = kBS * kD * 2;
 constexpr int kKStages = 3;                   // K tiles in flight (released when their S product is done)
 constexpr int kVStages = 3;                   // V tiles in flight (released when their PV product is done)
@@ -53,6 +57,12 @@ constexpr int kSBufs = 3;                     // TMEM S/P buffers (128 columns e
 // a 1 KB boundary (required by the 128-byte swizzle) and reports an error otherwise.
 constexpr int kSmemBytes = (1 + kKStages + kVStages) * kTileBytes;
 constexpr float kRescaleThreshold = 8.f;      // log2 units
+// A cluster is kCluster consecutive query tiles of one head and chunk.  They read the same K/V
+// tiles, so each CTA fetches a quarter of every tile's boxes and multicasts them to all: the
+// per-SM TMA work per tile drops by kCluster (one SM's TMA unit, not HBM or L2, bounds a
+// CTA that fetches all sixteen 4 KB boxes of a K+V tile itself).
+constexpr int kCluster = 4;
+constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
 
 struct PrefillParams {
   void* out;
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_k_full[kKStages], bar_k_empty[kKStages], bar_v_full[kVStages],
-      bar_v_empty[kVStages], bar_s_full[kSBufs], bar_p_full[kSBufs], bar_pv_done;
+      bar_v_empty[kVStages], bar_s_full[kSBufs], bar_p_full[kSBufs], bar_pv_done[kSBufs];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float row_xchg[2][2][kTile];                    // [use parity][half][row]: values the softmax halves swap
   __shared__ __align__(8) uint64_t bar_xchg[2];              // 256 arrivals: both halves have written
@@ -89,16 +99,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = p.cu_q_lens[c];
   const int qlen = p.cu_q_lens[c + 1] - q0;
   const int r0 = qt * kTile;
-  if (qlen <= 0 || r0 >= qlen) return;                       // no rows for this CTA
+  // Decisions before the first cluster barrier must be the same for the whole cluster.
+  const int r0_cl = (qt & ~(kCluster - 1)) * kTile;           // first row of the cluster
+  if (qlen <= 0 || r0_cl >= qlen) return;                    // no rows for the whole cluster
   const int start = p.q_start_pos[c];
   const int ctx = start + qlen;                              // keys 0 .. ctx-1 exist
   if (start < 0 || ctx > p.max_blocks * p.block_size) {
     if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
     return;
   }
-  const int row_hi = min(qlen, r0 + kTile);
-  const int kmax = start + row_hi;                           // keys needed: 0 .. kmax-1
+  // Every CTA of the cluster walks the keys the cluster needs; a CTA whose rows end earlier
+  // finds the extra keys in its rows' future, where the causal mask zeroes them.  A CTA with
+  // no rows at all still takes part (its outputs are not stored).
+  const int kmax = start + min(qlen, r0_cl + kCluster * kTile);
   const int nt = (kmax + kTile - 1) / kTile;
+  const uint32_t crank = cluster_ctarank();
   const int G = p.num_heads / p.num_kv_heads;
   const int h = hq / G;
   const int nb = (ctx + kBS - 1) / kBS;
@@ -119,13 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
     mbar_init(&bar_q, 1);
+    // A stage is free again once every CTA of the cluster has released it.
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bar_k_full[i], 1);
-      mbar_init(&bar_k_empty[i], 1);
+      mbar_init(&bar_k_empty[i], kCluster);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bar_v_full[i], 1);
-      mbar_init(&bar_v_empty[i], 1);
+      mbar_init(&bar_v_empty[i], kCluster);
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bar_s_full[i], 1);
@@ -133,7 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bar_xchg[0], 256);
     mbar_init(&bar_xchg[1], 256);
-    mbar_init(&bar_pv_done, 1);
+    // PV_t's completion arrives on bar_pv_done[t % kSBufs].  A waiter for PV_t is always at most
+    // one phase behind that barrier (PV_{t+kSBufs} needs P_{t+kSBufs}, which the softmax has not
+    // produced yet), so waiting by phase parity is exact.  One barrier for every PV would not
+    // be: the softmax checks it only now and then, and the barrier can run two phases ahead.
+    for (int i = 0; i < kSBufs; ++i) mbar_init(&bar_pv_done[i], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -142,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();                                            // every peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tO = tmem + 128 * kSBufs;
@@ -184,14 +205,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     Window wk{load_window(0), load_window(1), 0};
     Window wv = wk;
-    // The 8 lanes that hold the tile's block rows issue one box each, in the same instruction.
-    auto issue_tile = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, Window& win, int j) {
-      seek(win, j);
+    // The 8 lanes that hold the tile's block rows issue its boxes that fall to this CTA
+    // (box % kCluster == rank), multicast to the whole cluster, in the same instruction.
+    // Each CTA's own full barrier expects the whole tile, most of it sent by its peers.
+    auto issue_k = [&](uint8_t* dst, uint64_t* bar, int j) {
+      seek(wk, j);
       const int first = (8 * j) % 32;
       if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
       __syncwarp();
-      if (lane >= first && lane < first + kTile / kBS)
-        tma_load_3d(dst + (lane - first) * kBlockBytes, map, bar, 0, win.cur, 0, pol_kv);
+      const int blk = lane - first;
+      if (blk >= 0 && blk < kTile / kBS) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (uint32_t((2 * blk + hf) % kCluster) == crank)
+            tma_load_3d_mc(dst + hf * kHalfBytes + blk * (kBlockBytes / 2), &tmk, bar, 0, wk.cur, hf, kClusterMask,
+                           pol_kv);
+        }
+      }
+    };
+    auto issue_v = [&](uint8_t* dst, uint64_t* bar, int j) {
+      seek(wv, j);
+      const int first = (8 * j) % 32;
+      if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
+      __syncwarp();
+      const int blk = lane - first;
+      if (blk >= 0 && blk < kTile / kBS && uint32_t(blk % kCluster) == crank)
+        tma_load_3d_mc(dst + blk * kBlockBytes, &tmv, bar, 0, wv.cur, 0, kClusterMask, pol_kv);
     };
     // K runs ahead of V; each is issued as soon as its stage has been released.  Lane 0
     // polls the barriers and broadcasts, so the warp stays converged.
@@ -206,12 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && (kj < nt || vj < nt)) {
       bool progress = false;
       if (kj < nt && (kj < kKStages || ready(&bar_k_empty[kj % kKStages], uint32_t((kj - kKStages) / kKStages) & 1u))) {
-        issue_tile(&tmk, sK + (kj % kKStages) * kTileBytes, &bar_k_full[kj % kKStages], wk, kj);
+        issue_k(sK + (kj % kKStages) * kTileBytes, &bar_k_full[kj % kKStages], kj);
         ++kj;
         progress = true;
       }
       if (vj < kj && (vj < kVStages || ready(&bar_v_empty[vj % kVStages], uint32_t((vj - kVStages) / kVStages) & 1u))) {
-        issue_tile(&tmv, sV + (vj % kVStages) * kTileBytes, &bar_v_full[vj % kVStages], wv, vj);
+        issue_v(sV + (vj % kVStages) * kTileBytes, &bar_v_full[vj % kVStages], vj);
         ++vj;
         progress = true;
       }
@@ -231,19 +270,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
     }
-    // Drain: the last load of each stage must have landed before the CTA may exit.
+    // Drain: the last load of each stage must have landed, and every peer's release of the
+    // last tiles must have reached this CTA's barriers, before the CTA may leave the cluster.
     if (lane == 0) {
       for (int j = kj - kKStages < 0 ? 0 : kj - kKStages; j < kj; ++j)
         (void)mbar_wait(&bar_k_full[j % kKStages], uint32_t(j / kKStages) & 1u);
       for (int j = vj - kVStages < 0 ? 0 : vj - kVStages; j < vj; ++j)
         (void)mbar_wait(&bar_v_full[j % kVStages], uint32_t(j / kVStages) & 1u);
+      for (int j = kj - kKStages < 0 ? 0 : kj - kKStages; j < kj; ++j)
+        (void)mbar_wait(&bar_k_empty[j % kKStages], uint32_t(j / kKStages) & 1u);
+      for (int j = vj - kVStages < 0 ? 0 : vj - kVStages; j < vj; ++j)
+        (void)mbar_wait(&bar_v_empty[j % kVStages], uint32_t(j / kVStages) & 1u);
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     // S_j needs K_j and a free S buffer (PV_{j-2}, which reads P_{j-2} from that buffer,
     // issued: tcgen05 ops of one thread execute in order); PV_j needs P_j and V_j.  Whichever
     // is ready is issued first.
-    const uint32_t idesc_s = umma_idesc_f16(kBF16, 128, 64, false, false);
+    const uint32_t idesc_s = umma_idesc_f16(kBF16, 128, 128, false, false);
     const uint32_t idesc_o = umma_idesc_f16(kBF16, 128, 128, false, true);
     const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
     bool ok = mbar_wait(&bar_q, 0);
@@ -255,18 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int st = js % kKStages;
         const uint32_t tSj = tS(js);
-        // S columns 0..63 hold keys 16b + i (i < 8) of blocks b = 0..7, columns 64..127 keys
-        // 16b + 8 + i: in each set the 8-row groups of K sit 4 KB apart.
+        // k-step kk: dims 16kk .. 16kk + 15 of Q and K, both stored as [64-dim half][rows]
+        // with 8-row groups 1 KB apart, so S column n is key n of the tile.
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t qoff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * (kBlockBytes / 2) + (kk & 3) * 32;
-          const uint64_t qd = umma_sdesc_sw128(aQ + qoff, 16, 1024);
-          umma_f16(tSj, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff, 16, kBlockBytes), idesc_s, kk > 0);
-          umma_f16(tSj + 64, qd, umma_sdesc_sw128(aK + st * kTileBytes + koff + 1024, 16, kBlockBytes), idesc_s, kk > 0);
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          umma_f16(tSj, umma_sdesc_sw128(aQ + off, 16, 1024), umma_sdesc_sw128(aK + st * kTileBytes + off, 16, 1024),
+                   idesc_s, kk > 0);
         }
         umma_commit(&bar_s_full[js % kSBufs]);
-        umma_commit(&bar_k_empty[st]);
+        umma_commit_mc(&bar_k_empty[st], kClusterMask);     // released in every CTA of the cluster
         ++js;
         progress = true;
       }
@@ -276,16 +318,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = jp % kVStages;
         // P_jp sits in the first 64 columns of its S buffer, two 16-bit values per column.
         const uint32_t tP = tS(jp);
-        // k-step kk covers P columns 16kk .. 16kk + 15: blocks 2kk', 2kk' + 1 (kk' = kk % 4),
-        // rows 0..7 for kk < 4 and rows 8..15 after.
+        // k-step kk covers P columns 16kk .. 16kk + 15 = keys of block kk: its two 8-row
+        // groups sit 1 KB apart, its two 64-dim halves 2 KB apart.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t voff = (kk & 3) * 2 * kBlockBytes + (kk >> 2) * 1024;
-          umma_f16_ts(tO, tP + 8 * kk, umma_sdesc_sw128(aV + st * kTileBytes + voff, kBlockBytes / 2, kBlockBytes),
+          umma_f16_ts(tO, tP + 8 * kk, umma_sdesc_sw128(aV + st * kTileBytes + kk * kBlockBytes, kBlockBytes / 2, 1024),
                       idesc_o, jp > 0 || kk > 0);
         }
-        umma_commit(&bar_pv_done);
-        umma_commit(&bar_v_empty[st]);
+        umma_commit(&bar_pv_done[jp % kSBufs]);
+        umma_commit_mc(&bar_v_empty[st], kClusterMask);
         ++jp;
         progress = true;
       }
@@ -342,16 +383,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
       }
       tmem_wait_ld();
-      // Column i of this half holds key kb + 16 * (i / 8) + 8 * half + i % 8 (see the MMA).
-      const int lim = min(pos + 1, ctx) - (j * kTile + 8 * half);   // valid iff 16*(i/8) + i%8 < lim
+      // Column i of this half holds key kb + 64 * half + i.
+      const int lim = min(pos + 1, ctx) - (j * kTile + 64 * half);  // valid iff i < lim
       float mraw = -INFINITY;
-      if (lim >= kTile) {
+      if (lim >= 64) {                                       // all 64 columns of this half valid
 #pragma unroll
         for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, s[i]);
       } else {
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          s[i] = 16 * (i >> 3) + (i & 7) < lim ? s[i] : -INFINITY;
+          s[i] = i < lim ? s[i] : -INFINITY;
           mraw = fmaxf(mraw, s[i]);
         }
       }
@@ -361,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool grow = mt > m + kRescaleThreshold;          // also true for the first tile
       if (__any_sync(0xffffffffu, grow && j >= 1)) {
         // O must be up to date (the previous PV product done) before it is rescaled.
-        if (!(ok = mbar_wait(&bar_pv_done, uint32_t(j - 1) & 1u))) break;
+        if (!(ok = mbar_wait(&bar_pv_done[(j - 1) % kSBufs], uint32_t((j - 1) / kSBufs) & 1u))) break;
         __syncwarp();
         tc_fence_after();
         const float alpha = (grow && m != -INFINITY) ? fast_exp2(m - mt) : 1.f;
@@ -408,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar_p_full[j % kSBufs]);
     }
-    if (ok) ok = mbar_wait(&bar_pv_done, uint32_t(nt - 1) & 1u);
+    if (ok) ok = mbar_wait(&bar_pv_done[(nt - 1) % kSBufs], uint32_t((nt - 1) / kSBufs) & 1u);
     // Row sum = the two halves' partial sums (both used the same m).
     if (ok) {
       float other;
@@ -442,6 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
   }
   __syncthreads();
+  cluster_sync();                                            // no peer sends to this CTA any more
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -484,8 +526,8 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   const uint64_t rows = uint64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size;
   if (!encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT16, q, kD, uint64_t(num_heads), uint64_t(total_q), kD * 2,
                       uint64_t(num_heads) * kD * 2, 64, 1, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      // K / V as (64 dims, rows, 2 halves): one box = 16 rows of a block, both halves
-      !encode_tmap_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, k_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 2,
+      // K / V as (64 dims, rows, 2 halves): a K box is 16 rows of one half, a V box both halves
+      !encode_tmap_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, k_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 1,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, v_cache, 64, rows, 2, kD * 2, 128, 64, kBS, 2,
                       CU_TENSOR_MAP_SWIZZLE_128B))
@@ -508,7 +550,20 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   auto kern = q_dtype == PKV_BF16 ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return PKV_ERR_CUDA;
-  dim3 grid((max_q_len + kTile - 1) / kTile, num_heads, num_chunks);
-  kern<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tq, tk, tv, prm);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  // Query tiles rounded up to whole clusters; tiles past a chunk's rows only help fetch K/V.
+  const int qtiles = (max_q_len + kTile - 1) / kTile;
+  dim3 grid((qtiles + kCluster - 1) / kCluster * kCluster, num_heads, num_chunks);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

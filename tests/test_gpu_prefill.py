@@ -102,6 +102,19 @@ def test_block_size_32_chunks():
     _check(_case(5, [(37, 200), (0, 5), (300, 129), (1000, 1)], 8, 2, "bf16", nan_fill=True, bs=32))
 
 
+def test_single_row_chunks_after_long_prefixes_repeat_exactly():
+    """One query row whose keys end inside the last tile: the epilogue must see every PV
+    product of the row (the last ones finish after the softmax is done), on every run."""
+    c = _case(6, [(600, 1), (1000, 1), (77, 1), (3000, 1)], 8, 2, "bf16")
+    first = _check(c)
+    for _ in range(4):
+        out, err = _run(c)
+        assert err == 0
+        again, _ = _run(c)
+        assert torch.equal(out, again)
+    assert first <= TOL["bf16"]
+
+
 def test_gqa7_long_prefix():
     _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
 
