@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // polls the barriers and broadcasts, so the warp stays converged.
     auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
       uint32_t r = 0;
-      if (lane == 0) r = mbar_try_wait(bar, parity) ? 1u : 0u;
+      if (lane == 0) r = mbar_test(bar, parity) ? 1u : 0u;
       return __shfl_sync(0xffffffffu, r, 0) != 0;
     };
     int kj = 0, vj = 0;
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t t0 = 0;
     while (ok && jp < nt) {
       bool progress = false;
-      if (js < nt && js - jp < kSBufs && mbar_try_wait(&bar_k_full[js % kKStages], uint32_t(js / kKStages) & 1u)) {
+      if (js < nt && js - jp < kSBufs && mbar_test(&bar_k_full[js % kKStages], uint32_t(js / kKStages) & 1u)) {
         tc_fence_after();
         const int st = js % kKStages;
         const uint32_t tSj = tS(js);
@@ -312,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++js;
         progress = true;
       }
-      if (jp < js && mbar_try_wait(&bar_p_full[jp % kSBufs], uint32_t(jp / kSBufs) & 1u) &&
-          mbar_try_wait(&bar_v_full[jp % kVStages], uint32_t(jp / kVStages) & 1u)) {
+      if (jp < js && mbar_test(&bar_p_full[jp % kSBufs], uint32_t(jp / kSBufs) & 1u) &&
+          mbar_test(&bar_v_full[jp % kVStages], uint32_t(jp / kVStages) & 1u)) {
         tc_fence_after();
         const int st = jp % kVStages;
         // P_jp sits in the first 64 columns of its S buffer, two 16-bit values per column.
