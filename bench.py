@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture each), valid only for the
 # kernel source with this hash; when the source changes, traffic is reported as null until
 # re-measured.
-TRAFFIC = {"source_sha1": "382d42d9e8101985bf6f523f077974a7cae5b71e", "bytes_per_launch": 161459712}
+TRAFFIC = {"source_sha1": "f0762699157add3e84aca38b63606531653eac85", "bytes_per_launch": 161851136}
 
 
 def _src_hash() -> str:
