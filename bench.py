@@ -13,8 +13,9 @@ CUDA graph and replayed once between two events.  The decode kernel's own averag
 (split + merge, for its roofline) comes from a second graph of K decodes timed the same way.  Every step uses the next of
 R pool copies whose combined size is above 3x the L2 size, so no step finds its K/V in L2.
 `value` is device-resident throughput; `e2e` adds, every step, the pinned host->device
-copies of the step's inputs (q, new K/V, slots, tables, lengths) and the device->host copy
-of the output.
+copy of the step's inputs (q, new K/V, slots, tables, lengths, staged in one pinned buffer)
+and the device->host copy of the output, on copy streams that overlap the next step's upload
+and the previous step's download with the kernels (double-buffered inputs and outputs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -287,35 +288,73 @@ def run_gpu(args):
     assert pkv.pkv_get_device_error(stream) == 0
 
     # ---- end to end: host buffers, copies inside the timed region -----------------------
-    h_q = case.q.pin_memory()
-    h_kn = case.k_new.pin_memory()
-    h_vn = case.v_new.pin_memory()
-    h_slots = torch.tensor(plan.slots, dtype=torch.int64).pin_memory()
-    h_tables = torch.tensor(plan.tables, dtype=torch.int32).pin_memory()
-    h_lens = torch.tensor(plan.lens, dtype=torch.int32).pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_tables, h_lens))
-    d2h = h_out.numel() * h_out.element_size()
+    # A serving loop's shape: each step's inputs (q, new K/V, slots, tables, lengths) sit in one
+    # pinned staging buffer and go up in one copy; device inputs and outputs are double-
+    # buffered; uploads run on one copy stream and output downloads on another, ordered by
+    # events, so step k+1's upload and step k's download overlap step k's kernels.  Every step
+    # still moves its full input and output bytes across the host link.
+    host_parts = [case.q, case.k_new, case.v_new, torch.tensor(plan.slots, dtype=torch.int64),
+                  torch.tensor(plan.tables, dtype=torch.int32), torch.tensor(plan.lens, dtype=torch.int32)]
+    offs, pos = [], 0
+    for t in host_parts:
+        offs.append(pos)
+        pos += -(-t.numel() * t.element_size() // 256) * 256
+    h_in = torch.zeros(pos, dtype=torch.uint8).pin_memory()
+    for t, o in zip(host_parts, offs):
+        h_in[o:o + t.numel() * t.element_size()] = t.contiguous().view(-1).view(torch.uint8)
+    d_in = [torch.empty(pos, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def views(buf):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(host_parts, offs)]
+
+    dv = [views(d_in[i]) for i in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_parts)
+    d2h = h_outs[0].numel() * h_outs[0].element_size()
+    g_e2e = {}
+    for r in range(R):
+        for i in range(2):
+            qi, kni, vni, sli, tbi, lni = dv[i]
+            d_in[i].copy_(h_in)
+            gs = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gs, stream=stream, capture_error_mode="thread_local"):
+                pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r])
+                pkv.pkv_paged_decode(outs[i], qi, kcs[r], vcs[r], descs[r], tbi, lni, max_len, case.scale, part, ws)
+            g_e2e[(r, i)] = gs
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    step_done = [torch.cuda.Event() for _ in range(2)]
+    out_copied = [torch.cuda.Event() for _ in range(2)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         e_start.record(stream)
+        for ev in step_done + out_copied:
+            ev.record(stream)
         for k in range(K):
-            r = (W + k) % R
-            q.copy_(h_q, non_blocking=True)
-            k_new.copy_(h_kn, non_blocking=True)
-            v_new.copy_(h_vn, non_blocking=True)
-            slots.copy_(h_slots, non_blocking=True)
-            tables.copy_(h_tables, non_blocking=True)
-            lens.copy_(h_lens, non_blocking=True)
-            g_step[r].replay()
-            h_out.copy_(out, non_blocking=True)
+            i, r = k % 2, (W + k) % R
+            up.wait_event(step_done[i])                  # step k-2 no longer reads buffer i
+            with torch.cuda.stream(up):
+                d_in[i].copy_(h_in, non_blocking=True)
+                in_ready[i].record(up)
+            stream.wait_event(in_ready[i])
+            stream.wait_event(out_copied[i])             # step k-2's output has been read back
+            g_e2e[(r, i)].replay()
+            step_done[i].record(stream)
+            down.wait_event(step_done[i])
+            with torch.cuda.stream(down):
+                h_outs[i].copy_(outs[i], non_blocking=True)
+                out_copied[i].record(down)
+        for ev in out_copied:
+            stream.wait_event(ev)
         e_end.record(stream)
     stream.synchronize()
     barrier()
     e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
-    assert torch.equal(h_out.to(dev), out)
+    for i in range(2):
+        assert torch.equal(h_outs[i], out.cpu())
     pf_ms, pf_flops = prefill_measure(dev)
     sw_out, sw_in, sw_bytes = swap_measure(dev)
 
@@ -353,7 +392,9 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": {"value": round(aggregate_gbs(step_bytes, e2e_ms / K, ws_n), 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "per step one H2D of the pinned staged inputs and one D2H of the output, on two "
+                          "copy streams ordered by events; inputs and outputs double-buffered"},
         "prefill_chunk": {"workload": "mixed-step chunk: 512 causal rows at 3584..4095, 28/4 heads, bf16",
                           "bound": "tensor", "achieved": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1),
                           "peak": _bf16_peak(), "unit": "TFLOP/s",
