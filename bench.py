@@ -17,7 +17,10 @@ copy of the step's inputs (q, new K/V, slots, tables, lengths, staged in one pin
 and the device->host copy of the output, on copy streams that overlap the next step's upload
 and the previous step's download with the kernels (double-buffered inputs and outputs).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload 2|3|4|5]
+
+--workload picks another decode workload (3: 13B MHA, 4: long-context e4m3, 5: the mixed
+step's decode part); the default, 2, is the headline.
 """
 from __future__ import annotations
 
@@ -41,8 +44,17 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "paged-decode effective HBM GB/s (% of GB300 peak); seq-tokens attended/s"
-WORKLOAD = ("qwen2.5-7b-gqa paged decode step: 64 seqs, context_lens U[128,2048] (seed 1602), "
-            "28 q heads / 4 kv heads, head_dim 128, bf16, block_size 16, kv_write 64 tokens + paged_decode")
+WORKLOADS = {
+    2: "qwen2.5-7b-gqa paged decode step: 64 seqs, context_lens U[128,2048] (seed 1602), "
+       "28 q heads / 4 kv heads, head_dim 128, bf16, block_size 16, kv_write 64 tokens + paged_decode",
+    3: "13b-mha paged decode step: 256 seqs, lognormal context_lens (median 512, clipped to [16,8192], "
+       "seed 1603), 64 sharing a 1024-token prefix, 40/40 heads, head_dim 128, fp16, kv_write 256 tokens "
+       "+ paged_decode",
+    4: "long-context split-KV decode: 8 seqs of 32K..128K tokens (704,512 in all), 32 q heads / 8 kv heads, "
+       "head_dim 128, bf16 q, e4m3 KV with per-head scales, 512-token partitions, paged_decode only",
+    5: "mixed step's decode part: 128 seqs, context_lens U[256,4096] (seed 1605), 28/4 heads, head_dim 128, "
+       "bf16, kv_write 128 tokens + paged_decode (its 512-row chunk is the prefill_chunk line)",
+}
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -185,7 +197,7 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    case = synth.qwen7b_gqa_config()
+    case = synth.CONFIG_BUILDERS[args.workload]()
     t0 = time.perf_counter()
     plan = product_plan(case)
     host_plan_us = (time.perf_counter() - t0) * 1e6
@@ -198,24 +210,26 @@ def run_gpu(args):
     R = max(2, math.ceil(3 * l2 / pool_bytes) + 1)
     kcs = [case.k_cache.to(dev) for _ in range(R)]
     vcs = [case.v_cache.to(dev) for _ in range(R)]
-    desc = pkv.cache_desc(kcs[0])
-    descs = [pkv.cache_desc(k) for k in kcs]
+    k_scale = case.k_scale.to(dev) if case.k_scale is not None else None   # e4m3 caches: per-head scales
+    v_scale = case.v_scale.to(dev) if case.v_scale is not None else None
+    descs = [pkv.cache_desc(k, k_scale, v_scale) for k in kcs]
     q = case.q.to(dev)
-    k_new = case.k_new.to(dev)
-    v_new = case.v_new.to(dev)
+    k_new = case.k_new.to(dev) if case.writes else None
+    v_new = case.v_new.to(dev) if case.writes else None
     slots = torch.tensor(plan.slots, dtype=torch.int64, device=dev)
     tables = torch.tensor(plan.tables, dtype=torch.int32, device=dev)
     lens = torch.tensor(plan.lens, dtype=torch.int32, device=dev)
     out = torch.empty_like(q)
     max_len = max(plan.lens)
-    part = 0
+    part = case.partition_size
     wsb = pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim, 16,
                                          max_len, part)
     ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def write(r):
-        pkv.pkv_kv_write(k_new, v_new, slots, kcs[r], vcs[r], descs[r])
+        if case.writes:
+            pkv.pkv_kv_write(k_new, v_new, slots, kcs[r], vcs[r], descs[r])
 
     def decode(r):
         pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, part, ws)
@@ -293,8 +307,9 @@ def run_gpu(args):
     # buffered; uploads run on one copy stream and output downloads on another, ordered by
     # events, so step k+1's upload and step k's download overlap step k's kernels.  Every step
     # still moves its full input and output bytes across the host link.
-    host_parts = [case.q, case.k_new, case.v_new, torch.tensor(plan.slots, dtype=torch.int64),
-                  torch.tensor(plan.tables, dtype=torch.int32), torch.tensor(plan.lens, dtype=torch.int32)]
+    host_parts = [case.q, torch.tensor(plan.tables, dtype=torch.int32), torch.tensor(plan.lens, dtype=torch.int32)]
+    if case.writes:
+        host_parts += [case.k_new, case.v_new, torch.tensor(plan.slots, dtype=torch.int64)]
     offs, pos = [], 0
     for t in host_parts:
         offs.append(pos)
@@ -315,11 +330,13 @@ def run_gpu(args):
     g_e2e = {}
     for r in range(R):
         for i in range(2):
-            qi, kni, vni, sli, tbi, lni = dv[i]
+            qi, tbi, lni = dv[i][:3]
             d_in[i].copy_(h_in)
             gs = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gs, stream=stream, capture_error_mode="thread_local"):
-                pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r])
+                if case.writes:
+                    kni, vni, sli = dv[i][3:]
+                    pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r])
                 pkv.pkv_paged_decode(outs[i], qi, kcs[r], vcs[r], descs[r], tbi, lni, max_len, case.scale, part, ws)
             g_e2e[(r, i)] = gs
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -362,7 +379,8 @@ def run_gpu(args):
     ms_per_step = elapsed_ms / K
     value = aggregate_gbs(step_bytes, ms_per_step, ws_n)
     achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha1"] == _src_hash() else None
+    traffic = (TRAFFIC["bytes_per_launch"] if args.workload == 2 and TRAFFIC["source_sha1"] == _src_hash()
+               else None)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -374,9 +392,9 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3-kv/bf16" if case.kv_dtype == "e4m3" else case.kv_dtype,
         "data": "synthetic (seeded N(0,1) Q/K/V, shuffled physical block ids)",
-        "config": {"workload": WORKLOAD, "num_seqs": case.num_seqs, "attended_tokens": tokens,
+        "config": {"workload": WORKLOADS[args.workload], "num_seqs": case.num_seqs, "attended_tokens": tokens,
                    "step_bytes": step_bytes, "decode_bytes": decode_bytes, "kv_write_bytes": write_bytes,
                    "pool_copies": R, "l2": f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB > 3x L2)",
                    "launch": "one CUDA graph of K steps (kv_write, decode, merge per step; programmatic dependent launches)",
@@ -404,7 +422,7 @@ def run_gpu(args):
                         "bytes_per_call": sw_bytes, "device_to_host_gbs": round(sw_out, 1),
                         "host_to_device_gbs": round(sw_in, 1)},
         "host_plan_us": round(host_plan_us, 1),
-        "gpu_launches": 3 * K,                       # kv_write, decode, merge per timed step
+        "gpu_launches": (3 if case.writes else 2) * K,   # (kv_write,) decode, merge per timed step
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -498,22 +516,35 @@ def swap_measure(dev, n_blocks: int = 4096, iters: int = 10):
 
 
 def _oracle_step(case, plan, seqs):
-    """The oracle (as it stands) on a subset of the step: its KV write and decode."""
+    """The oracle (as it stands) on a subset of the step: its KV write and decode.  The sampled
+    sequences' blocks are gathered into a pool of their own first (tables and slots renumbered),
+    so the oracle's copy-on-return KV write copies only that pool."""
     import numpy as np
     from oracle import cache_ops, paged_attention as pa
     from tests.harness import codes, q_f64
-    k, v = codes(case.k_cache), codes(case.v_cache)
-    k, v = cache_ops.kv_write(k, v, codes(case.k_new)[seqs], codes(case.v_new)[seqs], [plan.slots[i] for i in seqs])
-    q = q_f64(case.q)[seqs]
-    pa.decode_attention(q, k, v, case.kv_dtype, [plan.tables[i] for i in seqs], [plan.lens[i] for i in seqs],
-                        case.scale)
+    bs = case.block_size
+    used = sorted({b for i in seqs for b in plan.tables[i] if b >= 0})
+    new_id = {b: n for n, b in enumerate(used)}
+    k, v = codes(case.k_cache)[used], codes(case.v_cache)[used]
+    tables = [[new_id[b] for b in plan.tables[i] if b >= 0] for i in seqs]
+    if case.writes:
+        slots = [new_id[plan.slots[i] // bs] * bs + plan.slots[i] % bs for i in seqs]
+        k, v = cache_ops.kv_write(k, v, codes(case.k_new)[seqs], codes(case.v_new)[seqs], slots)
+    ks = case.k_scale.numpy().astype(np.float64) if case.k_scale is not None else None
+    vs = case.v_scale.numpy().astype(np.float64) if case.v_scale is not None else None
+    pa.decode_attention(q_f64(case.q)[seqs], k, v, case.kv_dtype, tables, [plan.lens[i] for i in seqs], case.scale,
+                        ks, vs)
 
 
 def _sample_bytes(case, plan, seqs):
+    """Algorithmic bytes of the sampled sequences' share of the step (their rows counted per
+    sequence, as the oracle reads them)."""
     Hkv, D = case.num_kv_heads, case.head_dim
+    kv_elt = 1 if case.kv_dtype == "e4m3" else 2
     rows = sum(plan.lens[i] for i in seqs)
-    return (2 * rows * Hkv * D * 2 + 2 * len(seqs) * case.num_heads * D * 2 + 4 * len(seqs)
-            + 2 * 2 * len(seqs) * Hkv * D * 2 + 8 * len(seqs)), rows
+    n_w = len(seqs) if case.writes else 0
+    return (2 * rows * Hkv * D * kv_elt + 2 * len(seqs) * case.num_heads * D * 2 + 4 * len(seqs)
+            + 2 * 2 * n_w * Hkv * D * kv_elt + 8 * n_w), rows
 
 
 def cpu_baseline(case, plan, decode_bytes, write_bytes, budget_s: float = 12.0):
@@ -521,22 +552,23 @@ def cpu_baseline(case, plan, decode_bytes, write_bytes, budget_s: float = 12.0):
     seqs_all = list(range(case.num_seqs))
     done_bytes = done_tokens = 0
     n_seq = 0
+    per = 8 if max(plan.lens) <= 8192 else 1          # long sequences: one per oracle call
     t0 = time.perf_counter()
     if True:
         i = 0
         while time.perf_counter() - t0 < budget_s and n_seq < 4 * case.num_seqs:
-            seqs = [seqs_all[(i + j) % case.num_seqs] for j in range(8)]
+            seqs = [seqs_all[(i + j) % case.num_seqs] for j in range(per)]
             _oracle_step(case, plan, seqs)
             b, rows = _sample_bytes(case, plan, seqs)
             done_bytes += b
             done_tokens += rows
             n_seq += len(seqs)
-            i += 8
+            i += per
     dt = time.perf_counter() - t0
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "seq_tokens_per_s": round(done_tokens / dt, 1),
             "sample": f"fp64 numpy oracle (kv_write + decode) on {n_seq} sequence-steps of the same workload, "
-                      f"8 sequences per call, {dt:.1f} s wall, 1 BLAS thread"}
+                      f"{per} sequences per call, {dt:.1f} s wall, 1 BLAS thread"}
 
 
 def run_reference(args):
@@ -546,9 +578,9 @@ def run_reference(args):
     ws_n, rank, _ = _dist()
     if rank != 0:
         return
-    case = synth.qwen7b_gqa_config()
+    case = synth.CONFIG_BUILDERS[args.workload]()
     plan = oracle_plan(case)
-    per = 4
+    per = 4 if max(plan.lens) <= 8192 else 1
     if True:
         for k in range(args.warmup):
             _oracle_step(case, plan, [(k * per + j) % case.num_seqs for j in range(per)])
@@ -565,7 +597,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws_n,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "sample_per_step": f"{per} sequences"},
+            "data": "synthetic", "config": {"workload": WORKLOADS[args.workload], "sample_per_step": f"{per} sequences"},
             "seq_tokens_per_s": round(tot_rows / dt, 1),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"{per} sequences of the workload per step (kv_write + decode), fp64 numpy, "
@@ -580,6 +612,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS),
+                    help="2: the 7B GQA decode step (default, the headline); 3-5: the other decode workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
