@@ -142,6 +142,32 @@ def test_block_size_32(name, lens, hq, hkv, d, qd, kd, part):
     _check_case(case)
 
 
+def _random_decode_shape(seed):
+    """A seeded random decode configuration within the supported envelope."""
+    rng = np.random.default_rng(seed)
+    kd = ["f16", "bf16", "e4m3"][seed % 3]
+    d = 128 if kd == "e4m3" else int(rng.choice([64, 128]))
+    qd = "bf16" if kd == "bf16" else ("f16" if kd == "f16" else str(rng.choice(["f16", "bf16"])))
+    hkv = int(rng.integers(1, 5))
+    g = int(rng.integers(1, 9))
+    bs = int(rng.choice([16, 32]))
+    n = int(rng.integers(1, 40))
+    lens = [int(x) for x in rng.integers(0, 1500, n)]
+    lens[int(rng.integers(0, n))] = int(rng.integers(1, 3))             # a very short one
+    part = int(rng.choice([0, 0, 16, 48, 256]))
+    return f"rand{seed}", lens, g * hkv, hkv, d, qd, kd, part, bs
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes(seed):
+    """Random group sizes, head dims, dtypes, splits, block sizes and ragged lengths (some
+    sequences may be empty), with NaN in every unused pool row."""
+    name, lens, hq, hkv, d, qd, kd, part, bs = _random_decode_shape(seed)
+    case = synth.make_decode_case(name, 900 + seed, lens, hq, hkv, d, qd, kd, block_size=bs, partition_size=part,
+                                  unused_fill="nan")
+    _check_case(case)
+
+
 @pytest.mark.parametrize("kd", ["bf16", "e4m3"])
 def test_unused_slots_hold_nan(kd):
     """Rows past each sequence's end hold NaN; they must never reach the output."""

@@ -115,6 +115,18 @@ def test_single_row_chunks_after_long_prefixes_repeat_exactly():
     assert first <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_chunks(seed):
+    """Random chunk counts, prefixes, lengths, head groups and block sizes, NaN in unused rows."""
+    rng = np.random.default_rng(seed)
+    chunks = [(int(rng.integers(0, 1200)), int(rng.integers(1, 300))) for _ in range(int(rng.integers(1, 5)))]
+    hkv = int(rng.integers(1, 3))
+    hq = hkv * int(rng.integers(1, 9))
+    dtype = ["bf16", "f16"][seed % 2]
+    bs = [16, 32][(seed // 2) % 2]
+    _check(_case(10 + seed, chunks, hq, hkv, dtype, nan_fill=True, bs=bs), rows_per_chunk=list(range(0, 300, 7)))
+
+
 def test_gqa7_long_prefix():
     _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
 
