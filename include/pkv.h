@@ -240,6 +240,14 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtype q
  */
 PKV_API pkv_status pkv_get_device_error(int* code, pkv_stream_t stream);
 
+/*
+ * Diagnostic of the failure path every kernel shares: one warp waits on an mbarrier that
+ * nothing arrives on, with the same bounded wait the kernels use, for limit_ns (0 < limit_ns
+ * <= 1 s), then sets PKV_DEVERR_TIMEOUT and returns.  Nothing faults or hangs; the context
+ * stays usable.  Read the bit with pkv_get_device_error.
+ */
+PKV_API pkv_status pkv_check_bounded_wait(uint64_t limit_ns, pkv_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * Host block manager ("PagedAttention: manage the KV cache like virtual memory" §3.2–§3.3;
  * Lecture 33 §2.2, §2.4).  A FIFO free-block queue (allocate pops the head, free pushes

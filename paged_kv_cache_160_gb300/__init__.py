@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     DEVERR,
     cache_desc,
     lib,
+    pkv_check_bounded_wait,
     pkv_copy_blocks,
     pkv_decode_workspace_bytes,
     pkv_get_device_error,

@@ -51,6 +51,8 @@ def _load() -> ctypes.CDLL:
                                  POINTER(CacheDesc), c_void_p]
     lib.pkv_copy_blocks.restype = S
     lib.pkv_copy_blocks.argtypes = [c_void_p, c_void_p, POINTER(CacheDesc), c_void_p, c_int, c_void_p]
+    lib.pkv_check_bounded_wait.restype = S
+    lib.pkv_check_bounded_wait.argtypes = [ctypes.c_uint64, c_void_p]
     lib.pkv_swap_blocks.restype = S
     lib.pkv_swap_blocks.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, POINTER(CacheDesc),
                                     c_void_p, c_int, c_void_p]
@@ -190,6 +192,11 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, desc: CacheDes
     _check(lib.pkv_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
                                _dev(block_pairs, "block_pairs"), block_pairs.shape[0], _stream(stream)),
            "pkv_copy_blocks")
+
+
+def pkv_check_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Run the shared bounded wait on a barrier nothing arrives on; it sets the timeout bit."""
+    _check(lib.pkv_check_bounded_wait(int(limit_ns), _stream(stream)), "pkv_check_bounded_wait")
 
 
 def _dev_or_pinned(t: torch.Tensor, name: str) -> int:

@@ -3,6 +3,7 @@
 // so the library also loads on machines without a GPU driver).
 #include <mutex>
 
+#include "pkv_device.cuh"
 #include "pkv_host.h"
 
 namespace {
@@ -141,3 +142,28 @@ pkv_status pkv_get_device_error(int* code, pkv_stream_t stream) {
 }
 
 }  // extern "C"
+
+namespace {
+
+// One warp waits on an mbarrier that nothing arrives on, with the bounded wait every kernel
+// of the library uses; when the limit passes it reports PKV_DEVERR_TIMEOUT and returns.
+__global__ void bounded_wait_check_kernel(uint64_t limit_ns, unsigned* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    pkv::mbar_init(&bar, 1);
+    pkv::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool done = pkv::mbar_wait(&bar, 0, limit_ns);
+  if (!done && threadIdx.x == 0) pkv::set_error(err, PKV_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_check_bounded_wait(uint64_t limit_ns, pkv_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > pkv::kWaitLimitNs) return PKV_ERR_INVALID_ARG;
+  unsigned* err = pkv::error_word_ptr();
+  if (!err) return PKV_ERR_CUDA;
+  bounded_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

@@ -62,6 +62,9 @@ def test_argument_checks_run_on_host_without_gpu():
     assert L.pkv_swap_blocks(16, 16, 0, 16, 16, 8, ctypes.byref(desc), 16, 2, None) == 1
     assert L.pkv_swap_blocks(16, 16, 8, 16, 16, 8, ctypes.byref(desc), None, 2, None) == 1
     assert L.pkv_swap_blocks(16, 16, 8, 16, 16, 8, ctypes.byref(desc), 16, 0, None) == 0
+    # the bounded-wait diagnostic takes a limit in (0, 1 s]
+    assert L.pkv_check_bounded_wait(0, None) == 1
+    assert L.pkv_check_bounded_wait(2_000_000_000, None) == 1
 
 
 # ---------------------------------------------------------------------------------------

@@ -212,6 +212,22 @@ def test_workspace_needs_no_init_and_repeat_is_deterministic():
     assert pkv.pkv_get_device_error() == 0
 
 
+def test_a_wait_that_runs_out_reports_a_timeout_and_the_context_survives():
+    """The bounded wait every kernel uses, on a barrier nothing arrives on: after 2 ms it
+    gives up, sets the timeout bit, and later calls on the same context still work."""
+    import time
+    import paged_kv_cache_160_gb300 as pkv
+    pkv.pkv_get_device_error()
+    t0 = time.perf_counter()
+    pkv.pkv_check_bounded_wait(2_000_000)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 1.0
+    assert pkv.pkv_get_device_error() == pkv.DEVERR["timeout"]
+    assert pkv.pkv_get_device_error() == 0                  # reading clears the word
+    case = synth.make_decode_case("after_timeout", 84, [5, 40], 4, 2, 64, "f16", "f16")
+    _check_case(case)
+
+
 def test_device_checks_flag_bad_tables_without_faulting():
     import paged_kv_cache_160_gb300 as pkv
     case = synth.make_decode_case("bad", 81, [40, 40], 4, 4, 64, "f16", "f16", write=False)
