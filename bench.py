@@ -373,7 +373,7 @@ def run_gpu(args):
     for i in range(2):
         assert torch.equal(h_outs[i], out.cpu())
     pf_ms, pf_flops = prefill_measure(dev)
-    sw_out, sw_in, sw_bytes = swap_measure(dev)
+    sw_out, sw_in, sw_bytes, sw_link = swap_measure(dev)
 
     peak, peak_kind = _peaks()
     ms_per_step = elapsed_ms / K
@@ -420,7 +420,9 @@ def run_gpu(args):
                           "avg_launch_ms": round(pf_ms, 5), "flops_per_launch": pf_flops},
         "swap_blocks": {"workload": "4096 scattered blocks of the 7B layout (K and V), device <-> pinned host",
                         "bytes_per_call": sw_bytes, "device_to_host_gbs": round(sw_out, 1),
-                        "host_to_device_gbs": round(sw_in, 1)},
+                        "host_to_device_gbs": round(sw_in, 1),
+                        "contiguous_copy_gbs": {"device_to_host": round(sw_link[0], 1),
+                                                "host_to_device": round(sw_link[1], 1)}},
         "host_plan_us": round(host_plan_us, 1),
         "gpu_launches": (3 if case.writes else 2) * K,   # (kv_write,) decode, merge per timed step
         "clocks": clk.summary(),
@@ -512,7 +514,21 @@ def swap_measure(dev, n_blocks: int = 4096, iters: int = 10):
         res.append(a.elapsed_time(b) / iters)
     assert pkv.pkv_get_device_error(s) == 0
     nbytes = 2 * kc.numel() * kc.element_size()
-    return nbytes / (res[0] * 1e-3) / 1e9, nbytes / (res[1] * 1e-3) / 1e9, nbytes
+    # The host link's reference: the same bytes as one contiguous copy each way (copy engines).
+    flat_d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    link = []
+    for dst, src in ((flat_h, flat_d), (flat_d, flat_h)):
+        with torch.cuda.stream(s):
+            dst.copy_(src, non_blocking=True)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(iters):
+                dst.copy_(src, non_blocking=True)
+            b.record(s)
+        s.synchronize()
+        link.append(nbytes / (a.elapsed_time(b) / iters * 1e-3) / 1e9)
+    return nbytes / (res[0] * 1e-3) / 1e9, nbytes / (res[1] * 1e-3) / 1e9, nbytes, link
 
 
 def _oracle_step(case, plan, seqs):
