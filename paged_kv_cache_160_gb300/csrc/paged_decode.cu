@@ -589,6 +589,7 @@ constexpr int kMergeWarps = 8;
 template <int QT, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) split_kv_merge_kernel(const MergeParams p) {
   griddep_wait();                            // the decode kernel's partials are complete
+  griddep_launch_dependents();               // the next kernel may start its own prologue
   constexpr int kLanesPerHead = D / 4;       // 16-byte chunks of one head's row
   constexpr int kHP = 32 / kLanesPerHead;    // rows per load instruction of the warp
   constexpr int kChunk = 16;                 // loads in flight per lane
