@@ -62,7 +62,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture each), valid only for the
 # kernel source with this hash; when the source changes, traffic is reported as null until
 # re-measured.
-TRAFFIC = {"source_sha1": "f0762699157add3e84aca38b63606531653eac85", "bytes_per_launch": 161851136}
+TRAFFIC = {"source_sha1": "cbd31c39a7a3da0c813fb5614ca72c9a0675bfe9", "bytes_per_launch": 161682432}
 
 
 def _src_hash() -> str:
