@@ -170,7 +170,8 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_k
  *   workspace       (device) >= pkv_decode_workspace_bytes(...) bytes
  * Supported: kv f16/bf16 with the same q dtype, or e4m3 kv with f16/bf16 q (the e4m3
  * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16 or 32;
- * num_heads / num_kv_heads in 1..8.
+ * num_heads / num_kv_heads in 1..8; num_kv_heads * num_seqs * ceil(L_max / 16) < 2^31, where
+ * L_max = min(max_context_len, max_blocks_per_seq * block_size) (else PKV_ERR_UNSUPPORTED).
  * Launch order: the decode kernel is launched as a programmatic dependent of the previous
  * kernel on `stream`.  If that kernel allows early dependent launch (pkv_kv_write does), the
  * decode kernel may already read context_lens and block_tables while it still runs; q, the

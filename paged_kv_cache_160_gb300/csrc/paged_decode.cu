@@ -87,12 +87,29 @@ struct Tile {
   int s, h, b, nb, len;
 };
 
-// Largest s in [0, S) with mult * cum[s] <= t.
-__device__ __forceinline__ int find_seq(const int* cum, int S, int64_t t, int mult) {
-  int lo = 0, hi = S - 1;
+// Largest s in [lo, hi] with mult * cum[s] <= t, given mult * cum[lo] <= t.  cum is a
+// non-decreasing prefix array whose scaled entries stay below 2^31 (checked on the host).
+__device__ __forceinline__ int find_seq(const int* cum, int lo, int hi, int t, int mult) {
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (int64_t(mult) * cum[mid] <= t) lo = mid; else hi = mid - 1;
+    if (mult * cum[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The same search over [0, S) done by a whole warp for one t: each round the 32 lanes probe
+// 32 evenly spaced candidates and a ballot keeps the chunk holding the answer, so S entries
+// take ceil(log32 S) rounds instead of log2 S dependent probes.
+__device__ __forceinline__ int find_seq_warp(const int* cum, int S, int t, int mult, int lane) {
+  int lo = 0, n = S;                         // the answer lies in [lo, lo + n); mult * cum[lo] <= t
+  while (n > 1) {
+    const int step = (n + 31) >> 5;
+    const int pos = lo + lane * step;
+    const bool ok = lane * step < n && mult * cum[pos] <= t;
+    const unsigned b = __ballot_sync(0xffffffffu, ok);   // lane 0 always holds: b != 0
+    const int k = 31 - __clz(b);
+    lo += k * step;
+    n = min(step, n - k * step);
   }
   return lo;
 }
@@ -140,6 +157,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int PB = p.part_blocks;
   int* cum_nb = reinterpret_cast<int*>(smem + kWarps * kStages * C::kStageBytes);   // [S + 1]
   int* cum_np = cum_nb + (S + 1);                                                    // [S + 1]
+  int* lenc = cum_np + (S + 1);                                                      // [S] clamped lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -154,6 +172,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   }
 
   // ---- per-CTA prefix sums of blocks (and partitions) per sequence ---------------------
+  // The lengths are read from global memory once; the clamped values stay in shared memory
+  // for the second pass and for every cursor step below.
   {
     const int per = (S + blockDim.x - 1) / blockDim.x;
     const int s0 = min(S, int(threadIdx.x) * per), s1 = min(S, s0 + per);
@@ -162,6 +182,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       const int L = p.context_lens[s];
       const int Lc = clamp_len(L, p.max_len);
       if (Lc != L) set_error(p.err, PKV_DEVERR_CONTEXT_LEN);
+      lenc[s] = Lc;
       const int nb = (Lc + kBS - 1) / kBS;
       a += nb;
       u += PB ? (nb + PB - 1) / PB : 0;
@@ -178,7 +199,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     for (int w = 0; w < warp; ++w) { ba += warp_tot[w]; bu += warp_tot[kWarps + w]; }
     int ra = ba + ia - a, ru = bu + iu - u;   // exclusive prefix at s0
     for (int s = s0; s < s1; ++s) {
-      const int nb = (clamp_len(p.context_lens[s], p.max_len) + kBS - 1) / kBS;
+      const int nb = (lenc[s] + kBS - 1) / kBS;
       cum_nb[s] = ra;
       cum_np[s] = ru;
       ra += nb;
@@ -203,10 +224,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
   };
 
-  const int64_t T = int64_t(Hkv) * cum_nb[S];
-  const int64_t U = int64_t(Hkv) * cum_np[S];
-  const int64_t nunits = PB ? U : T;
-  const int W = int(p.num_workers < nunits ? int64_t(p.num_workers) : nunits);
+  // Tile and unit counts stay below 2^31 (checked on the host), so the index arithmetic
+  // from here on is 32-bit.
+  const int T = Hkv * cum_nb[S];
+  const int U = Hkv * cum_np[S];
+  const int nunits = PB ? U : T;
+  const int W = min(p.num_workers, nunits);
   const int w = blockIdx.x * kWarps + warp;
   if (w >= W) {                              // no tiles for this warp
     griddep_wait();
@@ -215,29 +238,37 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     return;
   }
 
-  auto locate = [&](int64_t t) -> Tile {
+  // Cursor of tile t, searching sequences lo..hi (which must hold it).
+  auto locate_in = [&](int t, int lo, int hi) -> Tile {
     Tile r;
-    r.s = find_seq(cum_nb, S, t, Hkv);
+    r.s = find_seq(cum_nb, lo, hi, t, Hkv);
     r.nb = cum_nb[r.s + 1] - cum_nb[r.s];
-    const int64_t off = t - int64_t(Hkv) * cum_nb[r.s];
-    r.h = int(off / r.nb);
-    r.b = int(off - int64_t(r.h) * r.nb);
-    r.len = clamp_len(p.context_lens[r.s], p.max_len);
+    const int off = t - Hkv * cum_nb[r.s];
+    r.h = off / r.nb;
+    r.b = off - r.h * r.nb;
+    r.len = lenc[r.s];
     return r;
   };
-  // First tile of unit u (partition mode) in the flattened tile order.
-  auto unit_tile = [&](int64_t u) -> int64_t {
+  auto locate = [&](int t) -> Tile {         // whole warp, same t
+    const int s = find_seq_warp(cum_nb, S, t, Hkv, lane);
+    return locate_in(t, s, s);
+  };
+  // First tile of unit u (partition mode) in the flattened tile order; whole warp.
+  auto unit_tile = [&](int u) -> int {
     if (u >= U) return T;
-    const int s = find_seq(cum_np, S, u, Hkv);
+    const int s = find_seq_warp(cum_np, S, u, Hkv, lane);
     const int np = cum_np[s + 1] - cum_np[s];
     const int nb = cum_nb[s + 1] - cum_nb[s];
-    const int64_t off = u - int64_t(Hkv) * cum_np[s];
-    const int h = int(off / np), part = int(off - int64_t(h) * np);
-    return int64_t(Hkv) * cum_nb[s] + int64_t(h) * nb + int64_t(part) * PB;
+    const int off = u - Hkv * cum_np[s];
+    const int h = off / np, part = off - h * np;
+    return Hkv * cum_nb[s] + h * nb + part * PB;
   };
-  auto start_of = [&](int64_t wi) -> int64_t { return wi * nunits / W; };
+  // Worker wi starts at unit floor(wi * nunits / W).  With nunits = uq * W + ur that is
+  // wi * uq + floor(wi * ur / W), and wi * ur < W^2 fits 32 unsigned bits.
+  const unsigned uq = unsigned(nunits) / unsigned(W), ur = unsigned(nunits) % unsigned(W);
+  auto start_of = [&](int wi) -> int { return int(unsigned(wi) * uq + unsigned(wi) * ur / unsigned(W)); };
 
-  int64_t t_begin, t_end;
+  int t_begin, t_end;
   if (PB) {
     t_begin = unit_tile(start_of(w));
     t_end = unit_tile(start_of(w + 1));
@@ -245,7 +276,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     t_begin = start_of(w);
     t_end = start_of(w + 1);
   }
-  const int n = int(t_end - t_begin);
+  const int n = t_end - t_begin;
+  const Tile first = locate(t_begin);
+  const Tile last = locate(t_end - 1);
 
   uint8_t* my_stages = smem + warp * kStages * C::kStageBytes;
   const uint64_t pol = l2_policy_evict_first();
@@ -260,17 +293,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     do { ++c.s; } while (c.s < S && cum_nb[c.s + 1] == cum_nb[c.s]);
     if (c.s < S) {
       c.nb = cum_nb[c.s + 1] - cum_nb[c.s];
-      c.len = clamp_len(p.context_lens[c.s], p.max_len);
+      c.len = lenc[c.s];
     }
   };
 
   // Block ids of the worker's tiles, 32 per window: lane l holds the id of tile
   // 32 * window + l of the range.  The next window is loaded one window ahead so the
-  // table lookups never sit on the path from one TMA issue to the next.
+  // table lookups never sit on the path from one TMA issue to the next.  The range's tiles
+  // lie in sequences first.s .. last.s, so each lane searches only those.
   auto load_window = [&](int win) -> int {
-    const int64_t t = t_begin + int64_t(win) * 32 + lane;
+    const int t = t_begin + win * 32 + lane;
     if (t >= t_end) return -1;
-    const Tile c = locate(t);
+    const Tile c = locate_in(t, first.s, last.s);
     return p.block_tables[int64_t(c.s) * p.max_blocks + (c.b >> p.tile_shift)];
   };
   int bid_cur = load_window(0);                // in flight while the piece count below is worked out
@@ -282,25 +316,26 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   // so it is worked out before the wait.
   int last_np = 1;
   if (lane == 0) {
-    const Tile c = locate(t_end - 1);
+    const Tile& c = last;
     const int64_t u_end = PB ? int64_t(Hkv) * cum_np[c.s] + int64_t(c.h) * (cum_np[c.s + 1] - cum_np[c.s]) +
                                    (c.nb - 1) / PB
                              : int64_t(Hkv) * cum_nb[c.s] + int64_t(c.h) * c.nb + c.nb - 1;
     last_np = int(((u_end + 1) * W - 1) / nunits) - w + 1;
   }
 
-  // Issues the TMA loads of the worker's tile j (cursor c) into stage st; lane 0 records in
-  // `valid` (bit st) whether the tile's block id was inside the pool.  Whole warp calls it.
+  // First pool row of tile c in block pb: the (block, kv head) rows start at
+  // (pb * Hkv + h) * block_size and a 32-token block holds the tile's 16 rows at offset 0
+  // or 16.  -1 marks a block id outside the pool.
+  auto tile_row = [&](const Tile& c, int pb) -> int {
+    if (pb < 0 || pb >= p.num_blocks) return -1;
+    return int((int64_t(pb) * Hkv + c.h) * p.block_size + (c.b & ((1 << p.tile_shift) - 1)) * kBS);
+  };
+  // Lane 0 starts the TMA loads of one tile (pool row y) into stage st and records in
+  // `valid` (bit st) whether the tile's block id was inside the pool.
   uint32_t valid = 0;
-  auto issue = [&](const Tile& c, int j, int st) {
-    if (j % 32 == 0 && j > 0) {
-      bid_cur = bid_nxt;
-      bid_nxt = load_window(j / 32 + 1);
-    }
-    const int pb = __shfl_sync(0xffffffffu, bid_cur, j % 32);
-    if (lane != 0) return;
+  auto launch_tile = [&](int y, int st) {
     uint64_t* bar = &bars[warp][st];
-    if (pb < 0 || pb >= p.num_blocks) {
+    if (y < 0) {
       set_error(p.err, PKV_DEVERR_BLOCK_ID);
       valid &= ~(1u << st);
       mbar_arrive(bar);                      // completes the phase without data
@@ -308,9 +343,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     valid |= 1u << st;
     mbar_arrive_expect_tx(bar, C::kStageBytes);
-    // First pool row of the tile: the (block, kv head) rows start at (pb * Hkv + h) * block_size
-    // and a 32-token block holds the tile's 16 rows at offset 0 or 16.
-    const int y = int((int64_t(pb) * Hkv + c.h) * p.block_size + (c.b & ((1 << p.tile_shift) - 1)) * kBS);
     uint8_t* kdst = my_stages + st * C::kStageBytes;
     if constexpr (C::kNBox == 2) {
       // One 3-D box brings both 128-byte halves of the 16 rows: [half 0: 16 x 128 B][half 1].
@@ -321,31 +353,48 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       tma_load_2d(kdst + C::kTileBytes, &tmv, bar, 0, y, pol);
     }
   };
+  // Issues the worker's tile j (cursor c) into stage st.  Whole warp calls it.
+  auto issue = [&](const Tile& c, int j, int st) {
+    if (j % 32 == 0 && j > 0) {
+      bid_cur = bid_nxt;
+      bid_nxt = load_window(j / 32 + 1);
+    }
+    const int pb = __shfl_sync(0xffffffffu, bid_cur, j % 32);
+    if (lane == 0) launch_tile(tile_row(c, pb), st);
+  };
+
+  // Pool rows of the first kStages tiles, so that only the TMA issue itself follows the wait.
+  Tile pc = first;                           // producer cursor, kStages tiles ahead
+  int y0[kStages];
+#pragma unroll
+  for (int i = 0; i < kStages; ++i) {
+    const int pb = __shfl_sync(0xffffffffu, bid_cur, i);
+    y0[i] = tile_row(pc, pb);
+    if (i + 1 < kStages && i + 1 < n) advance(pc);
+  }
 
   // Up to here the kernel has read only lengths and block tables.  The cache, the queries,
   // the outputs and the workspace are touched only after the preceding kernel on the stream
   // (typically the KV write of this step) has finished.
   griddep_wait();
   griddep_launch_dependents();
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kStages; ++i)
+      if (i < n) launch_tile(y0[i], i);
+  }
+  if (n > kStages - 1) advance(pc);          // pc now points at tile kStages of the range
   zero_empty();
 
   // The query rows of the segment this range ends in are read only when that piece starts,
   // late in the range: bring them into L1 now so the switch does not wait on memory.
-  if (t_end - 1 - t_begin >= 1) {
-    const Tile a = locate(t_begin), b = locate(t_end - 1);
-    if (a.s != b.s || a.h != b.h) {
-      const int qbytes = G * D * 2;                      // f16 / bf16 queries
-      const uint8_t* qrow0 = static_cast<const uint8_t*>(p.q) + (int64_t(b.s) * Hkv + b.h) * G * D * 2;
-      for (int off = lane * 128; off < qbytes; off += 32 * 128) prefetch_l1(qrow0 + off);
-    }
+  if (first.s != last.s || first.h != last.h) {
+    const int qbytes = G * D * 2;                      // f16 / bf16 queries
+    const uint8_t* qrow0 = static_cast<const uint8_t*>(p.q) + (int64_t(last.s) * Hkv + last.h) * G * D * 2;
+    for (int off = lane * 128; off < qbytes; off += 32 * 128) prefetch_l1(qrow0 + off);
   }
 
-  Tile pc = locate(t_begin);                 // producer cursor, kStages tiles ahead
-  for (int i = 0; i < min(n, kStages); ++i) {
-    issue(pc, i, i);
-    advance(pc);
-  }
-  Tile tl = locate(t_begin);                 // consumer cursor
+  Tile tl = first;                           // consumer cursor
 
   // Per-piece state.
   uint32_t qf[C::kKSteps][2];
@@ -700,7 +749,7 @@ size_t dynamic_smem_limit(K kern) {
 
 template <int KV, int D, int NW, int NS>
 size_t smem_bytes(int num_seqs) {
-  return 1024 + size_t(NW) * NS * Cfg<KV, D>::kStageBytes + 2 * sizeof(int) * size_t(num_seqs + 1);
+  return 1024 + size_t(NW) * NS * Cfg<KV, D>::kStageBytes + 3 * sizeof(int) * size_t(num_seqs + 1);
 }
 
 template <int KV, int QT, int D, int NW, int NS>
@@ -793,7 +842,12 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   if (int64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size >= (int64_t(1) << 31))
     return PKV_ERR_UNSUPPORTED;
 
+  // The kernel indexes tiles (16 rows of one kv head) and workers in 32 bits.
+  const int64_t max_len = std::min<int64_t>(int64_t(max_blocks_per_seq) * cache->block_size, max_context_len);
+  if (int64_t(cache->num_kv_heads) * num_seqs * ((max_len + kBS - 1) / kBS) >= (int64_t(1) << 31))
+    return PKV_ERR_UNSUPPORTED;
   const int grid = decode_grid();
+  if (int64_t(grid) * kMaxWarps >= (int64_t(1) << 16)) return PKV_ERR_UNSUPPORTED;
   const int part_blocks = partition_size / kBS;
   const int64_t slots = num_slots(grid * kMaxWarps);
   const Layout lay = layout(num_seqs, cache->num_kv_heads, group, D, slots);
@@ -831,7 +885,7 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   prm.num_kv_heads = cache->num_kv_heads;
   prm.group = group;
   prm.max_blocks = max_blocks_per_seq;
-  prm.max_len = int(std::min<int64_t>(int64_t(max_blocks_per_seq) * cache->block_size, max_context_len));
+  prm.max_len = int(max_len);
   prm.num_blocks = cache->num_blocks;
   prm.block_size = cache->block_size;
   prm.tile_shift = cache->block_size == 32 ? 1 : 0;
