@@ -62,7 +62,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture each), valid only for the
 # kernel source with this hash; when the source changes, traffic is reported as null until
 # re-measured.
-TRAFFIC = {"source_sha1": "cbd31c39a7a3da0c813fb5614ca72c9a0675bfe9", "bytes_per_launch": 161682432}
+TRAFFIC = {"source_sha1": "bd8f055ea42932ee06ecf674fc122281dd99d3b8", "bytes_per_launch": 161774592}
 
 
 def _src_hash() -> str:
@@ -188,7 +188,7 @@ def run_gpu(args):
 
     import paged_kv_cache_160_gb300 as pkv
     import synth
-    from tests.harness import product_plan
+    from tests.harness import append_slots, product_plan
 
     ws_n, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -227,6 +227,10 @@ def run_gpu(args):
     ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
+    # Every decode token goes to its sequence's last position, so the step's write is fused
+    # into the decode call (pkv_paged_decode_append); the unfused pair is timed beside it.
+    fused = case.writes and append_slots(case, plan) == list(plan.slots)
+
     def write(r):
         if case.writes:
             pkv.pkv_kv_write(k_new, v_new, slots, kcs[r], vcs[r], descs[r])
@@ -234,11 +238,19 @@ def run_gpu(args):
     def decode(r):
         pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, part, ws)
 
+    def step(r, fuse=fused):
+        if fuse:
+            pkv.pkv_paged_decode_append(out, q, k_new, v_new, kcs[r], vcs[r], descs[r], tables, lens, max_len,
+                                        case.scale, part, ws)
+        else:
+            write(r)
+            decode(r)
+
     # eager warm-up (also initialises the library's per-device state before capture)
     with torch.cuda.stream(stream):
         for r in range(R):
-            write(r)
-            decode(r)
+            step(r, False)
+            step(r)
     stream.synchronize()
     assert pkv.pkv_get_device_error(stream) == 0
     K, W = args.steps, args.warmup
@@ -248,32 +260,29 @@ def run_gpu(args):
             import torch.distributed as dist
             dist.barrier()
 
-    # The timed loop is one CUDA graph of K steps (each: kv_write -> decode -> split-KV merge,
-    # the last two launched as programmatic dependents), rotating over the pool copies.  The
-    # decode kernel's own average duration (split + merge, for its roofline) is timed the same
-    # way on a graph of K decodes alone; event nodes between kernels would break the
-    # programmatic launches and inflate it.
-    def capture(n_steps, first, with_write=True):
+    # The timed loop is one CUDA graph of K steps (each: the fused append + decode -> split-KV
+    # merge, or kv_write -> decode -> merge, launched as programmatic dependents), rotating over
+    # the pool copies.  The decode kernel's own average duration (decode + merge, without the
+    # write, for its roofline) is timed the same way on a graph of K decodes alone; event nodes
+    # between kernels would break the programmatic launches and inflate it.
+    def capture(n_steps, first, kind="step"):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
             for k in range(n_steps):
                 r = (first + k) % R
-                if with_write:
-                    write(r)
-                decode(r)
+                if kind == "step":
+                    step(r)
+                elif kind == "unfused":
+                    step(r, False)
+                else:
+                    decode(r)
         return g
 
     g_warm = capture(W, 0)
     g_timed = capture(K, W)
-    g_dec_warm = capture(W, 0, with_write=False)
-    g_dec = capture(K, W, with_write=False)
-    g_step = []                                          # single steps, for the e2e loop
-    for r in range(R):
-        gs = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gs, stream=stream, capture_error_mode="thread_local"):
-            write(r)
-            decode(r)
-        g_step.append(gs)
+    g_dec_warm = capture(W, 0, kind="step" if fused else "decode")   # the step's decode call alone
+    g_dec = capture(K, W, kind="step" if fused else "decode")
+    g_unf = capture(K, W, kind="unfused") if fused else None
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -297,6 +306,16 @@ def run_gpu(args):
             g_dec.replay()
             d_end.record(stream)
         stream.synchronize()
+        unfused_ms = None
+        if g_unf is not None:
+            u_start, u_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g_warm.replay()
+                u_start.record(stream)
+                g_unf.replay()
+                u_end.record(stream)
+            stream.synchronize()
+            unfused_ms = u_start.elapsed_time(u_end) / K
     elapsed_ms = max_over_ranks(start.elapsed_time(end), dev)
     dec_avg_ms = d_start.elapsed_time(d_end) / K
     assert pkv.pkv_get_device_error(stream) == 0
@@ -309,7 +328,9 @@ def run_gpu(args):
     # still moves its full input and output bytes across the host link.
     host_parts = [case.q, torch.tensor(plan.tables, dtype=torch.int32), torch.tensor(plan.lens, dtype=torch.int32)]
     if case.writes:
-        host_parts += [case.k_new, case.v_new, torch.tensor(plan.slots, dtype=torch.int64)]
+        host_parts += [case.k_new, case.v_new]
+        if not fused:
+            host_parts.append(torch.tensor(plan.slots, dtype=torch.int64))
     offs, pos = [], 0
     for t in host_parts:
         offs.append(pos)
@@ -327,45 +348,63 @@ def run_gpu(args):
     h_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_parts)
     d2h = h_outs[0].numel() * h_outs[0].element_size()
-    g_e2e = {}
-    for r in range(R):
-        for i in range(2):
-            qi, tbi, lni = dv[i][:3]
-            d_in[i].copy_(h_in)
-            gs = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gs, stream=stream, capture_error_mode="thread_local"):
-                if case.writes:
-                    kni, vni, sli = dv[i][3:]
-                    pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r])
-                pkv.pkv_paged_decode(outs[i], qi, kcs[r], vcs[r], descs[r], tbi, lni, max_len, case.scale, part, ws)
-            g_e2e[(r, i)] = gs
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    step_done = [torch.cuda.Event() for _ in range(2)]
-    out_copied = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_graph(n_steps, first):
+        """n_steps serving steps captured in one graph: per step, the H2D of the staged
+        inputs (upload stream), the step's kernels, and the D2H of its output (download
+        stream), with events giving the double-buffer order."""
+        g = torch.cuda.CUDAGraph()
+        evs = []
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            up.wait_event(fork)
+            down.wait_event(fork)
+            for k in range(n_steps):
+                i, r = k % 2, (first + k) % R
+                in_ready, step_done, out_copied = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+                if k >= 2:
+                    up.wait_event(evs[k - 2][1])             # step k-2 no longer reads buffer i
+                with torch.cuda.stream(up):
+                    d_in[i].copy_(h_in, non_blocking=True)
+                    in_ready.record(up)
+                stream.wait_event(in_ready)
+                if k >= 2:
+                    stream.wait_event(evs[k - 2][2])         # step k-2's output has been read back
+                qi, tbi, lni = dv[i][:3]
+                if fused:
+                    kni, vni = dv[i][3:5]
+                    pkv.pkv_paged_decode_append(outs[i], qi, kni, vni, kcs[r], vcs[r], descs[r], tbi, lni, max_len,
+                                                case.scale, part, ws)
+                else:
+                    if case.writes:
+                        kni, vni, sli = dv[i][3:]
+                        pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r])
+                    pkv.pkv_paged_decode(outs[i], qi, kcs[r], vcs[r], descs[r], tbi, lni, max_len, case.scale,
+                                         part, ws)
+                step_done.record(stream)
+                down.wait_event(step_done)
+                with torch.cuda.stream(down):
+                    h_outs[i].copy_(outs[i], non_blocking=True)
+                    out_copied.record(down)
+                evs.append((in_ready, step_done, out_copied))
+            for ev in evs[-2:]:
+                stream.wait_event(ev[2])
+            join = torch.cuda.Event()
+            join.record(up)
+            stream.wait_event(join)
+        return g
+
+    g_e2e_warm = e2e_graph(W, 0)
+    g_e2e = e2e_graph(K, W)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
+        g_e2e_warm.replay()
         e_start.record(stream)
-        for ev in step_done + out_copied:
-            ev.record(stream)
-        for k in range(K):
-            i, r = k % 2, (W + k) % R
-            up.wait_event(step_done[i])                  # step k-2 no longer reads buffer i
-            with torch.cuda.stream(up):
-                d_in[i].copy_(h_in, non_blocking=True)
-                in_ready[i].record(up)
-            stream.wait_event(in_ready[i])
-            stream.wait_event(out_copied[i])             # step k-2's output has been read back
-            g_e2e[(r, i)].replay()
-            step_done[i].record(stream)
-            down.wait_event(step_done[i])
-            with torch.cuda.stream(down):
-                h_outs[i].copy_(outs[i], non_blocking=True)
-                out_copied[i].record(down)
-        for ev in out_copied:
-            stream.wait_event(ev)
+        g_e2e.replay()
         e_end.record(stream)
     stream.synchronize()
     barrier()
@@ -378,7 +417,8 @@ def run_gpu(args):
     peak, peak_kind = _peaks()
     ms_per_step = elapsed_ms / K
     value = aggregate_gbs(step_bytes, ms_per_step, ws_n)
-    achieved = decode_bytes / (dec_avg_ms * 1e-3) / 1e9
+    roof_bytes = step_bytes if fused else decode_bytes        # the fused call also moves the new rows
+    achieved = roof_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = (TRAFFIC["bytes_per_launch"] if args.workload == 2 and TRAFFIC["source_sha1"] == _src_hash()
                else None)
     line = {
@@ -397,22 +437,30 @@ def run_gpu(args):
         "config": {"workload": WORKLOADS[args.workload], "num_seqs": case.num_seqs, "attended_tokens": tokens,
                    "step_bytes": step_bytes, "decode_bytes": decode_bytes, "kv_write_bytes": write_bytes,
                    "pool_copies": R, "l2": f"rotating {R} pool copies ({R * pool_bytes / 1e6:.0f} MB > 3x L2)",
-                   "launch": "one CUDA graph of K steps (kv_write, decode, merge per step; programmatic dependent launches)",
+                   "launch": ("one CUDA graph of K steps (fused kv write + decode, then merge, per step; "
+                              "programmatic dependent launches)" if fused else
+                              "one CUDA graph of K steps (kv_write, decode, merge per step; programmatic "
+                              "dependent launches)"),
+                   "step_kind": "pkv_paged_decode_append + merge" if fused else
+                                ("pkv_kv_write + pkv_paged_decode + merge" if case.writes else
+                                 "pkv_paged_decode + merge"),
                    "partition_size": part,
                    "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
         "seq_tokens_per_s": round(ws_n * tokens / (ms_per_step * 1e-3), 1),
         "pct_of_nominal_8tbs": round(100 * value / ws_n / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_copy": round(100 * value / ws_n / peak, 2),
-        "roofline": {"kernel": "paged_decode", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"kernel": "paged_decode_append (decode + merge)" if fused else "paged_decode (decode + merge)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": {"value": round(aggregate_gbs(step_bytes, e2e_ms / K, ws_n), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": "per step one H2D of the pinned staged inputs and one D2H of the output, on two "
-                          "copy streams ordered by events; inputs and outputs double-buffered"},
+                          "copy streams ordered by events; inputs and outputs double-buffered; the K steps "
+                          "(copies and kernels) replayed as one CUDA graph"},
         "prefill_chunk": {"workload": "mixed-step chunk: 512 causal rows at 3584..4095, 28/4 heads, bf16",
                           "bound": "tensor", "achieved": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1),
                           "peak": _bf16_peak(), "unit": "TFLOP/s",
@@ -424,7 +472,10 @@ def run_gpu(args):
                         "contiguous_copy_gbs": {"device_to_host": round(sw_link[0], 1),
                                                 "host_to_device": round(sw_link[1], 1)}},
         "host_plan_us": round(host_plan_us, 1),
-        "gpu_launches": (3 if case.writes else 2) * K,   # (kv_write,) decode, merge per timed step
+        "gpu_launches": (3 if case.writes and not fused else 2) * K,   # (kv_write,) decode, merge per step
+        "unfused_step": None if unfused_ms is None else {
+            "ms_per_step": round(unfused_ms, 5), "value": round(aggregate_gbs(step_bytes, unfused_ms, 1), 1),
+            "what": "the same step as pkv_kv_write + pkv_paged_decode (3 launches), one graph of K steps"},
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -442,7 +493,7 @@ def prefill_measure(dev, iters: int = 30):
     import torch
     import paged_kv_cache_160_gb300 as pkv
     import synth
-    from tests.harness import product_plan
+    from tests.harness import append_slots, product_plan
     case = synth.mixed_config()
     plan = product_plan(case)
     ch = case.chunk
@@ -570,16 +621,15 @@ def cpu_baseline(case, plan, decode_bytes, write_bytes, budget_s: float = 12.0):
     n_seq = 0
     per = 8 if max(plan.lens) <= 8192 else 1          # long sequences: one per oracle call
     t0 = time.perf_counter()
-    if True:
-        i = 0
-        while time.perf_counter() - t0 < budget_s and n_seq < 4 * case.num_seqs:
-            seqs = [seqs_all[(i + j) % case.num_seqs] for j in range(per)]
-            _oracle_step(case, plan, seqs)
-            b, rows = _sample_bytes(case, plan, seqs)
-            done_bytes += b
-            done_tokens += rows
-            n_seq += len(seqs)
-            i += per
+    i = 0
+    while time.perf_counter() - t0 < budget_s:         # about budget_s of CPU work
+        seqs = [seqs_all[(i + j) % case.num_seqs] for j in range(per)]
+        _oracle_step(case, plan, seqs)
+        b, rows = _sample_bytes(case, plan, seqs)
+        done_bytes += b
+        done_tokens += rows
+        n_seq += len(seqs)
+        i += per
     dt = time.perf_counter() - t0
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "seq_tokens_per_s": round(done_tokens / dt, 1),

@@ -187,6 +187,29 @@ PKV_API pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype,
                             pkv_stream_t stream);
 
 /*
+ * paged_decode_append: pkv_kv_write of one new token per sequence fused into
+ * pkv_paged_decode (PagedAttention §3.3: each new token fills its sequence's last block).
+ * For every sequence i with L = context_lens[i] >= 1, the new rows k_new[i] and v_new[i] are
+ * stored at position L - 1, i.e. slot block_tables[i][(L - 1) / B] * B + (L - 1) % B, quantised
+ * to e4m3 with k_scale / v_scale for an e4m3 cache exactly as pkv_kv_write does, and the decode
+ * then attends positions 0 .. L - 1, the new one included.  Caches and out are bit-identical to
+ * pkv_kv_write (with those slots) followed by pkv_paged_decode.
+ *   k_new, v_new  (device) [num_seqs][num_kv_heads][head_dim] of q_dtype, 16-byte aligned
+ *   k_cache, v_cache  (device) written at those positions only
+ * Sequences with L == 0 write nothing.  A length above the clamp bound (see pkv_paged_decode)
+ * writes nothing and is flagged PKV_DEVERR_CONTEXT_LEN; a block id outside the pool writes
+ * nothing and is flagged PKV_DEVERR_BLOCK_ID.  The written block must not be shared with
+ * another sequence of the call (copy-on-write has run), as for pkv_kv_write.  Other
+ * arguments, limits, launch order and results as pkv_paged_decode.
+ */
+PKV_API pkv_status pkv_paged_decode_append(void* out, const void* q, pkv_dtype q_dtype, int num_seqs,
+                                   int num_heads, const void* k_new, const void* v_new, void* k_cache,
+                                   void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int max_context_len, float scale, int partition_size, void* workspace,
+                                   size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * paged_decode for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that must not allocate at decode
  * time: a plain C host without a device allocator of its own for scratch space, or a

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     pkv_get_device_error,
     pkv_kv_write,
     pkv_paged_decode,
+    pkv_paged_decode_append,
     pkv_paged_decode_noalloc,
     pkv_noalloc_scratch_bytes,
     pkv_paged_prefill_chunk,

@@ -62,6 +62,10 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_decode.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                      POINTER(CacheDesc), c_void_p, c_int, c_void_p, c_int, c_float, c_int,
                                      c_void_p, c_size_t, c_void_p]
+    lib.pkv_paged_decode_append.restype = S
+    lib.pkv_paged_decode_append.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                            c_void_p, POINTER(CacheDesc), c_void_p, c_int, c_void_p, c_int, c_float,
+                                            c_int, c_void_p, c_size_t, c_void_p]
     lib.pkv_noalloc_scratch_bytes.restype = c_size_t
     lib.pkv_noalloc_scratch_bytes.argtypes = []
     lib.pkv_paged_decode_noalloc.restype = S
@@ -236,6 +240,25 @@ def pkv_paged_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, 
                                 int(partition_size), _dev(workspace, "workspace"),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "pkv_paged_decode")
+
+
+def pkv_paged_decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                            k_cache: torch.Tensor, v_cache: torch.Tensor, desc: CacheDesc, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, max_context_len: int, scale: float, partition_size: int,
+                            workspace: torch.Tensor, stream=None) -> None:
+    """Writes each sequence's new K/V row (k_new, v_new: [num_seqs, num_kv_heads, head_dim], q's dtype)
+    at position context_lens[i] - 1, then decodes as pkv_paged_decode."""
+    assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+    assert k_new.dtype == q.dtype and v_new.dtype == q.dtype and k_new.shape == v_new.shape
+    assert k_new.shape[0] == q.shape[0] and k_new.is_contiguous() and v_new.is_contiguous()
+    _check(lib.pkv_paged_decode_append(_dev(out, "out"), _dev(q, "q"), pkv_dtype_of(q), q.shape[0], q.shape[1],
+                                       _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+                                       _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                       _dev(block_tables, "block_tables"), block_tables.shape[1],
+                                       _dev(context_lens, "context_lens"), int(max_context_len), float(scale),
+                                       int(partition_size), _dev(workspace, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "pkv_paged_decode_append")
 
 
 def pkv_noalloc_scratch_bytes() -> int:

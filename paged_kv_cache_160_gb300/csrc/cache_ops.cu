@@ -51,13 +51,6 @@ __device__ __forceinline__ float2 load2(const void* p) {
   }
 }
 
-// Two fp32 values to two e4m3 codes (round to nearest even, saturate to +-448); lo -> low byte.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-  unsigned short r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // f16/bf16 rows into an e4m3 cache: code = e4m3(x / scale[h]); 16 codes per thread.
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads) kv_write_quant_kernel(

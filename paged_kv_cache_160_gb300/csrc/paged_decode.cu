@@ -50,6 +50,7 @@ struct Cfg {
   static constexpr int kElt = KV == KV_E4M3 ? 1 : 2;
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kNBox = kRowBytes / 128;       // 128-byte-wide TMA boxes per row
+  static constexpr int kRowChunks = kRowBytes / 16;   // 16-byte chunks per cache row
   static constexpr int kTileBytes = kBS * kRowBytes;  // one 16-row K (or V) tile
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kKSteps = D / 16;
@@ -81,6 +82,12 @@ struct DecodeParams {
   float2* ml;             // [slots][group] (running max in log2 units, sum of exponentials)
   float* po;              // [slots][group][D] unnormalised partial outputs
   unsigned* err;
+  // Fused append (null k_new: plain decode): each sequence's new K/V row, [num_seqs][num_kv_heads][D]
+  // in the q dtype, belongs at position context_len - 1; it is written to the caches and attended.
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
 };
 
 struct Tile {
@@ -430,6 +437,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       }
     }
 
+    // Fused append: the segment's last tile holds the new token's row.  Lane l < 2 * kRowChunks
+    // fetches 16 cache bytes' worth of it (K for the first half of the lanes, V for the rest)
+    // while the tile is still in flight.
+    const bool app = p.k_new != nullptr && tl.b + 1 == tl.nb;
+    uint4 na = make_uint4(0u, 0u, 0u, 0u), nb2 = make_uint4(0u, 0u, 0u, 0u);
+    int apb = -1, araw = -1;
+    if (app) {
+      araw = p.context_lens[tl.s];           // a clamped length has no new row to place
+      apb = p.block_tables[int64_t(tl.s) * p.max_blocks + ((tl.len - 1) >> (4 + p.tile_shift))];
+      if (lane < 2 * C::kRowChunks) {
+        const int c = lane % C::kRowChunks;
+        const uint4* src = static_cast<const uint4*>(lane < C::kRowChunks ? p.k_new : p.v_new) +
+                           ((int64_t(tl.s) * Hkv + tl.h) * D * 2) / 16 + c * (KV == KV_E4M3 ? 2 : 1);
+        na = src[0];
+        if constexpr (KV == KV_E4M3) nb2 = src[1];
+      }
+    }
+
     if (!mbar_wait(&bars[warp][st], uint32_t(i / kStages) & 1u)) {
       // Give up: report, then wait (bounded) for this warp's loads still in flight.
       if (lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -438,6 +463,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
 
     const bool ok = (__shfl_sync(0xffffffffu, valid, 0) >> st) & 1u;
+    if (app && ok && araw == tl.len) {
+      // Row r of the tile is position len - 1.  Put the new row into the staged tile (same
+      // swizzled layout as the TMA box) and into the cache at that position.
+      if (lane < 2 * C::kRowChunks) {
+        const bool isv = lane >= C::kRowChunks;
+        const int c = lane % C::kRowChunks;
+        const int r = (tl.len - 1) & (kBS - 1);
+        uint4 v = na;
+        if constexpr (KV == KV_E4M3) v = quant16_e4m3<QT == KV_BF16>(na, nb2, (isv ? p.v_scale : p.k_scale)[tl.h]);
+        const uint32_t tbase = smem_u32(my_stages + st * C::kStageBytes) + (isv ? C::kTileBytes : 0);
+        const uint32_t a = C::kNBox == 2 ? tbase + (c >> 3) * 2048 + swz128(r, c & 7) : tbase + swz128(r, c);
+        sts128(a, v.x, v.y, v.z, v.w);
+        fence_proxy_async_smem();                // orders this write before the stage's next TMA fill
+        const int64_t row = (int64_t(apb) * Hkv + tl.h) * p.block_size + ((tl.len - 1) & (p.block_size - 1));
+        static_cast<uint4*>(isv ? p.v_cache : p.k_cache)[row * C::kRowChunks + c] = v;
+      }
+      __syncwarp();
+    }
     const int nv = ok ? min(kBS, tl.len - tl.b * kBS) : 0;
     if (nv > 0) {
       const uint32_t kbase = smem_u32(my_stages + st * C::kStageBytes);
@@ -814,18 +857,25 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
   return layout(num_seqs, num_kv_heads, group, head_dim, slots).total;
 }
 
-pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
-                            const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
-                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-                            int max_context_len, float scale, int partition_size, void* workspace,
-                            size_t workspace_bytes, pkv_stream_t stream) {
-  using namespace pkv;
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Both decode entry points: plain (k_new == v_new == nullptr) or with the fused append.
+pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                       const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                       int max_context_len, float scale, int partition_size, void* workspace,
+                       size_t workspace_bytes, pkv_stream_t stream, const void* k_new, const void* v_new) {
   pkv_status st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || partition_size < 0)
     return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+  if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+    return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_INVALID_ARG;
@@ -895,6 +945,10 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
   prm.ml = reinterpret_cast<float2*>(ws + lay.ml);
   prm.po = reinterpret_cast<float*>(ws + lay.po);
   prm.err = err;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
+  prm.k_cache = const_cast<void*>(k_cache);
+  prm.v_cache = const_cast<void*>(v_cache);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool qbf = q_dtype == PKV_BF16;
@@ -910,6 +964,33 @@ pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num
                  : launch<KV_E4M3, KV_F16, 128>(prm, tk, tv, grid, s);
   }
   return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                            const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int max_context_len, float scale, int partition_size, void* workspace,
+                            size_t workspace_bytes, pkv_stream_t stream) {
+  return pkv::decode_impl(out, q, q_dtype, num_seqs, num_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, partition_size, workspace,
+                          workspace_bytes, stream, nullptr, nullptr);
+}
+
+pkv_status pkv_paged_decode_append(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                                   const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                   const pkv_cache_desc* cache, const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int max_context_len, float scale,
+                                   int partition_size, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+  return pkv::decode_impl(out, q, q_dtype, num_seqs, num_heads, k_cache, v_cache, cache, block_tables,
+                          max_blocks_per_seq, context_lens, max_context_len, scale, partition_size, workspace,
+                          workspace_bytes, stream, k_new, v_new);
 }
 
 }  // extern "C"

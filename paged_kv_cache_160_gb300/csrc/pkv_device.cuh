@@ -206,6 +206,35 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return y;
 }
 
+// Two fp32 values to two e4m3 codes (round to nearest even, saturate to +-448); lo -> low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16 f16/bf16 values (a: elements 0-7, b: 8-15) to 16 e4m3 codes of x / scale, in element
+// order.  The division is correctly rounded, so every writer of the cache agrees bit for bit.
+template <bool kBF16>
+__device__ __forceinline__ uint4 quant16_e4m3(const uint4 a, const uint4 b, float scale) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 lo, hi;
+    if constexpr (kBF16) {
+      lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * k]));
+      hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * k + 1]));
+    } else {
+      lo = __half22float2(*reinterpret_cast<const __half2*>(&w[2 * k]));
+      hi = __half22float2(*reinterpret_cast<const __half2*>(&w[2 * k + 1]));
+    }
+    r[k] = f32x2_to_e4m3x2(__fdiv_rn(lo.x, scale), __fdiv_rn(lo.y, scale)) |
+           (f32x2_to_e4m3x2(__fdiv_rn(hi.x, scale), __fdiv_rn(hi.y, scale)) << 16);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Two e4m3 codes (low byte -> low half) to two fp16 values; exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t out;

@@ -168,9 +168,22 @@ class DeviceResult:
     device_error: int
 
 
+def append_slots(case, plan: Plan) -> List[int]:
+    """Slot of position L - 1 of each decode sequence (L = its length after the step)."""
+    bs = case.block_size
+    return [plan.tables[i][(L - 1) // bs] * bs + (L - 1) % bs if L >= 1 else -1 for i, L in enumerate(plan.lens)]
+
+
 def device_run(case, plan: Plan, partition_size: Optional[int] = None, keep_intermediate: bool = True,
-               device: str = "cuda", run_prefill: bool = True) -> DeviceResult:
+               device: str = "cuda", run_prefill: bool = True, fused_append: bool = False,
+               append_inputs: Optional[Tuple[torch.Tensor, torch.Tensor]] = None) -> DeviceResult:
+    """fused_append: the decode tokens' K/V go through pkv_paged_decode_append instead of
+    pkv_kv_write + pkv_paged_decode (each decode token's slot must be its sequence's last
+    position).  append_inputs: the (k_new, v_new) the fused call gets, when they differ from the
+    case's stored codes (f16/bf16 rows that an e4m3 cache quantises)."""
     import paged_kv_cache_160_gb300 as pkv
+    if fused_append:
+        assert case.writes and append_slots(case, plan) == list(plan.slots), "slots are not the last positions"
     dev = torch.device(device)
     kc = case.k_cache.to(dev)
     vc = case.v_cache.to(dev)
@@ -179,10 +192,11 @@ def device_run(case, plan: Plan, partition_size: Optional[int] = None, keep_inte
     desc = pkv.cache_desc(kc, ks, vs)
     if plan.cows:
         pkv.pkv_copy_blocks(kc, vc, desc, torch.tensor(plan.cows, dtype=torch.int32, device=dev))
-    slots = list(plan.slots) + list(plan.chunk_slots)
+    dec_writes = case.writes and not fused_append
+    slots = (list(plan.slots) if dec_writes else []) + list(plan.chunk_slots)
     if slots:
-        kn = [case.k_new] if case.writes else []
-        vn = [case.v_new] if case.writes else []
+        kn = [case.k_new] if dec_writes else []
+        vn = [case.v_new] if dec_writes else []
         if case.chunk is not None:
             kn.append(case.chunk.k_new); vn.append(case.chunk.v_new)
         pkv.pkv_kv_write(torch.cat(kn).to(dev), torch.cat(vn).to(dev),
@@ -196,7 +210,12 @@ def device_run(case, plan: Plan, partition_size: Optional[int] = None, keep_inte
     ws_bytes = pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
                                               case.block_size, max_len, part)
     ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    pkv.pkv_paged_decode(out, q, kc, vc, desc, tables, lens, max_len, case.scale, part, ws)
+    if fused_append:
+        kn_, vn_ = append_inputs if append_inputs is not None else (case.k_new, case.v_new)
+        pkv.pkv_paged_decode_append(out, q, kn_.to(dev), vn_.to(dev), kc, vc, desc, tables, lens,
+                                    max_len, case.scale, part, ws)
+    else:
+        pkv.pkv_paged_decode(out, q, kc, vc, desc, tables, lens, max_len, case.scale, part, ws)
     pre = None
     if case.chunk is not None and run_prefill:
         cq = case.chunk.q.to(dev)
