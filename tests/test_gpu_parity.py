@@ -206,6 +206,10 @@ def test_workspace_needs_no_init_and_repeat_is_deterministic():
         out = torch.empty_like(q)
         pkv.pkv_paged_decode(out, q, kc, vc, desc, tables, lens, max(plan.lens), case.scale, part, ws)
         outs.append(out)
+        out2 = torch.empty_like(q)                                            # the same workspace again
+        pkv.pkv_paged_decode(out2, q, kc, vc, desc, tables, lens, max(plan.lens), case.scale, part, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out2, out)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
     assert (outs[3].float() - outs[0].float()).abs().max().item() < 2e-2
