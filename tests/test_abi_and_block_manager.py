@@ -51,6 +51,11 @@ def test_argument_checks_run_on_host_without_gpu():
     # tile indices must fit 32 bits: 4 kv heads x 65536 sequences x 8192 tiles = 2^31
     assert L.pkv_paged_decode(16, 16, 1, 65536, 8, 16, 16, ctypes.byref(desc), 16, 8192, 16, 131072, 0.1, 0, 16,
                               1 << 20, None) == 2
+    # fused append: both new-row pointers are required and 16-byte aligned
+    assert L.pkv_paged_decode_append(16, 16, 1, 4, 8, None, 16, 16, 16, ctypes.byref(desc), 16, 8, 16, 128, 0.1,
+                                     0, 16, 1 << 20, None) == 1
+    assert L.pkv_paged_decode_append(16, 16, 1, 4, 8, 16, 24, 16, 16, ctypes.byref(desc), 16, 8, 16, 128, 0.1,
+                                     0, 16, 1 << 20, None) == 1
     # misaligned pointer
     assert L.pkv_kv_write(17, 16, 1, 4, 16, 16, 16, ctypes.byref(desc), None) == 1
     # e4m3 cache without scales
