@@ -412,6 +412,8 @@ def run_gpu(args):
     for i in range(2):
         assert torch.equal(h_outs[i], out.cpu())
     pf_ms, pf_flops = prefill_measure(dev)
+    cache_ops = cache_ops_measure(pkv, case, plan, kcs[0], vcs[0], descs[0], k_new, v_new, slots, write_bytes,
+                                  stream) if case.writes else None
     sw_out, sw_in, sw_bytes, sw_link = swap_measure(dev)
 
     peak, peak_kind = _peaks()
@@ -471,6 +473,7 @@ def run_gpu(args):
                         "host_to_device_gbs": round(sw_in, 1),
                         "contiguous_copy_gbs": {"device_to_host": round(sw_link[0], 1),
                                                 "host_to_device": round(sw_link[1], 1)}},
+        "cache_ops": cache_ops,
         "host_plan_us": round(host_plan_us, 1),
         "gpu_launches": (3 if case.writes and not fused else 2) * K,   # (kv_write,) decode, merge per step
         "unfused_step": None if unfused_ms is None else {
@@ -484,6 +487,51 @@ def run_gpu(args):
     if ws_n > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def cache_ops_measure(pkv, case, plan, kc, vc, desc, k_new, v_new, slots, write_bytes, stream,
+                      iters: int = 50, pairs: int = 64):
+    """kv_write of the step's tokens and copy_blocks of `pairs` used blocks into free ones, each
+    timed alone: one CUDA graph of `iters` calls between two events.  Both are latency-bound
+    at these sizes (a few MB at most)."""
+    import torch
+    bs = case.block_size
+    used = set()
+    for row, L in zip(plan.tables, plan.lens):
+        used.update(row[:-(-L // bs)])
+    free = [b for b in range(case.num_blocks) if b not in used]
+    n = min(pairs, len(free))
+    src = sorted(used)[:n]
+    pr = torch.tensor(list(zip(src, free[:n])), dtype=torch.int32, device=kc.device)
+    block_bytes = kc[0].numel() * kc.element_size()
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for _ in range(iters):
+                fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) / iters
+
+    kw_ms = timed(lambda: pkv.pkv_kv_write(k_new, v_new, slots, kc, vc, desc))
+    cb_ms = timed(lambda: pkv.pkv_copy_blocks(kc, vc, desc, pr))
+    assert pkv.pkv_get_device_error(stream) == 0
+    cb_bytes = 2 * 2 * n * block_bytes                    # K and V blocks, read and written
+    return {"kv_write": {"tokens": len(plan.slots), "bytes": write_bytes, "avg_launch_ms": round(kw_ms, 5),
+                         "gbs": round(write_bytes / (kw_ms * 1e-3) / 1e9, 1)},
+            "copy_blocks": {"pairs": n, "bytes": cb_bytes, "avg_launch_ms": round(cb_ms, 5),
+                            "gbs": round(cb_bytes / (cb_ms * 1e-3) / 1e9, 1)},
+            "timing": f"one CUDA graph of {iters} back-to-back calls between events, per-call average"}
 
 
 def prefill_measure(dev, iters: int = 30):
