@@ -4,18 +4,21 @@ Workload: the Qwen2.5-7B-shaped GQA decode batch — 64 running sequences with c
 lengths uniform in [128, 2048], 28 query heads / 4 kv heads, head_dim 128, bf16 Q/K/V,
 16-token blocks in a shuffled pool ([num_blocks, 4, 16, 128], pool = blocks needed + 10%).
 One step = plan the step on the host block manager (done once; its cost is reported
-separately), kv_write of the 64 new tokens, then paged_decode over every sequence's
-L + 1 tokens (two launches: the split-KV decode, then the log-sum-exp merge of split
-segments as its programmatic dependent).
+separately), the write of the 64 new tokens' K/V, then paged_decode over every sequence's
+L + 1 tokens.  Every new token belongs at its sequence's last position, so the write is
+fused into the decode call (pkv_paged_decode_append: two launches, the split-KV decode and
+the log-sum-exp merge of split segments as its programmatic dependent); kv_write + decode
+is timed beside it.
 
 Timing: CUDA events on the launching stream.  The K timed steps are captured into one
-CUDA graph and replayed once between two events.  The decode kernel's own average duration
-(split + merge, for its roofline) comes from a second graph of K decodes timed the same way.  Every step uses the next of
-R pool copies whose combined size is above 3x the L2 size, so no step finds its K/V in L2.
-`value` is device-resident throughput; `e2e` adds, every step, the pinned host->device
-copy of the step's inputs (q, new K/V, slots, tables, lengths, staged in one pinned buffer)
-and the device->host copy of the output, on copy streams that overlap the next step's upload
-and the previous step's download with the kernels (double-buffered inputs and outputs).
+CUDA graph and replayed once between two events.  The decode call's own average duration
+(decode + merge, for its roofline) comes from a second graph of K calls timed the same way.
+Every step uses the next of R pool copies whose combined size is above 3x the L2 size, so
+no step finds its K/V in L2.  `value` is device-resident throughput.  `e2e` passes HOST
+buffers to the call: every step's inputs (q, new K/V, tables, lengths) are read in place
+from pinned host memory and its output is written to pinned host memory by the kernels,
+across NVLink-C2C.  The same steps with explicit staged H2D/D2H copies on copy streams are
+reported beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload 2|3|4|5]
 
@@ -320,7 +323,7 @@ def run_gpu(args):
     dec_avg_ms = d_start.elapsed_time(d_end) / K
     assert pkv.pkv_get_device_error(stream) == 0
 
-    # ---- end to end: host buffers, copies inside the timed region -----------------------
+    # ---- end to end, staged: explicit copies on copy streams --------------------------------
     # A serving loop's shape: each step's inputs (q, new K/V, slots, tables, lengths) sit in one
     # pinned staging buffer and go up in one copy; device inputs and outputs are double-
     # buffered; uploads run on one copy stream and output downloads on another, ordered by
@@ -408,9 +411,55 @@ def run_gpu(args):
         e_end.record(stream)
     stream.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
+    staged_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     for i in range(2):
         assert torch.equal(h_outs[i], out.cpu())
+
+    # Zero-copy (the headline e2e): the step's inputs sit in pinned host buffers that are
+    # passed to the call itself, and the kernels write the output straight into pinned host
+    # memory; Grace reaches both over NVLink-C2C, so every step still moves its input and
+    # output bytes across the host link, with no copy node breaking the programmatic launches.
+    # Two buffer sets alternate, as a serving loop's host would fill one while the other is read.
+    zero_copy = fused or not case.writes
+    if zero_copy:
+        hsets = []
+        for _ in range(2):
+            hs = {"q": case.q.clone().pin_memory(), "tb": torch.tensor(plan.tables, dtype=torch.int32).pin_memory(),
+                  "ln": torch.tensor(plan.lens, dtype=torch.int32).pin_memory(),
+                  "out": torch.empty(out.shape, dtype=out.dtype).pin_memory()}
+            if case.writes:
+                hs["kn"], hs["vn"] = case.k_new.clone().pin_memory(), case.v_new.clone().pin_memory()
+            hsets.append(hs)
+
+        def zc_graph(n_steps, first):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for k in range(n_steps):
+                    hs, r = hsets[k % 2], (first + k) % R
+                    if fused:
+                        pkv.pkv_paged_decode_append(hs["out"], hs["q"], hs["kn"], hs["vn"], kcs[r], vcs[r], descs[r],
+                                                    hs["tb"], hs["ln"], max_len, case.scale, part, ws)
+                    else:
+                        pkv.pkv_paged_decode(hs["out"], hs["q"], kcs[r], vcs[r], descs[r], hs["tb"], hs["ln"],
+                                             max_len, case.scale, part, ws)
+            return g
+
+        gz_warm, gz = zc_graph(W, 0), zc_graph(K, W)
+        z_start, z_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            gz_warm.replay()
+            z_start.record(stream)
+            gz.replay()
+            z_end.record(stream)
+        stream.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(z_start.elapsed_time(z_end), dev)
+        for hs in hsets:
+            assert torch.equal(hs["out"], out.cpu())
+    else:
+        e2e_ms = staged_ms
     pf_ms, pf_flops = prefill_measure(dev)
     cache_ops = cache_ops_measure(pkv, case, plan, kcs[0], vcs[0], descs[0], k_new, v_new, slots, write_bytes,
                                   stream) if case.writes else None
@@ -460,9 +509,16 @@ def run_gpu(args):
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": {"value": round(aggregate_gbs(step_bytes, e2e_ms / K, ws_n), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "per step one H2D of the pinned staged inputs and one D2H of the output, on two "
-                          "copy streams ordered by events; inputs and outputs double-buffered; the K steps "
-                          "(copies and kernels) replayed as one CUDA graph"},
+                "copies": ("the call gets HOST buffers: each step's inputs (q, new K/V, tables, lengths) are "
+                           "read in place from pinned host memory and its output is written to pinned host "
+                           "memory by the kernels (NVLink-C2C); two buffer sets alternate; the K steps are "
+                           "one CUDA graph") if zero_copy else
+                          ("per step one H2D of the pinned staged inputs and one D2H of the output, on two copy "
+                           "streams ordered by events; double-buffered; the K steps are one CUDA graph"),
+                "staged_copies": {"value": round(aggregate_gbs(step_bytes, staged_ms / K, ws_n), 1),
+                                  "ms_per_step": round(staged_ms / K, 5),
+                                  "what": "the same steps with explicit H2D/D2H copies on two copy streams, "
+                                          "ordered by events (double-buffered), in one CUDA graph"}},
         "prefill_chunk": {"workload": "mixed-step chunk: 512 causal rows at 3584..4095, 28/4 heads, bf16",
                           "bound": "tensor", "achieved": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1),
                           "peak": _bf16_peak(), "unit": "TFLOP/s",

@@ -168,6 +168,10 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_k
  *                  (and to max_blocks_per_seq * block_size) and flagged PKV_DEVERR_CONTEXT_LEN
  *   partition_size  0 = balanced split; else split granularity in tokens (multiple of 16)
  *   workspace       (device) >= pkv_decode_workspace_bytes(...) bytes
+ * out, q, block_tables and context_lens may instead be pinned host memory (cudaHostAlloc /
+ * cudaHostRegister, reachable through unified addressing): the kernels then read and write
+ * them in place over the host link, so a serving loop needs no separate copies.  The caches
+ * and the workspace must be device memory.
  * Supported: kv f16/bf16 with the same q dtype, or e4m3 kv with f16/bf16 q (the e4m3
  * path computes in fp16, so |q| must stay below 65504); head_dim 64/128; block_size 16 or 32;
  * num_heads / num_kv_heads in 1..8; num_kv_heads * num_seqs * ceil(L_max / 16) < 2^31, where
@@ -194,7 +198,8 @@ PKV_API pkv_status pkv_paged_decode(void* out, const void* q, pkv_dtype q_dtype,
  * to e4m3 with k_scale / v_scale for an e4m3 cache exactly as pkv_kv_write does, and the decode
  * then attends positions 0 .. L - 1, the new one included.  Caches and out are bit-identical to
  * pkv_kv_write (with those slots) followed by pkv_paged_decode.
- *   k_new, v_new  (device) [num_seqs][num_kv_heads][head_dim] of q_dtype, 16-byte aligned
+ *   k_new, v_new  (device, or pinned host memory as for q) [num_seqs][num_kv_heads][head_dim]
+ *                 of q_dtype, 16-byte aligned
  *   k_cache, v_cache  (device) written at those positions only
  * Sequences with L == 0 write nothing.  A length above the clamp bound (see pkv_paged_decode)
  * writes nothing and is flagged PKV_DEVERR_CONTEXT_LEN; a block id outside the pool writes

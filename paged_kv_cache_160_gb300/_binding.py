@@ -232,11 +232,12 @@ def pkv_decode_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int,
 def pkv_paged_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                      desc: CacheDesc, block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
                      scale: float, partition_size: int, workspace: torch.Tensor, stream=None) -> None:
+    """out, q, block_tables and context_lens may be pinned host memory (read and written in place)."""
     assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
-    _check(lib.pkv_paged_decode(_dev(out, "out"), _dev(q, "q"), pkv_dtype_of(q), q.shape[0], q.shape[1],
-                                _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
-                                _dev(block_tables, "block_tables"), block_tables.shape[1],
-                                _dev(context_lens, "context_lens"), int(max_context_len), float(scale),
+    _check(lib.pkv_paged_decode(_dev_or_pinned(out, "out"), _dev_or_pinned(q, "q"), pkv_dtype_of(q), q.shape[0],
+                                q.shape[1], _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                _dev_or_pinned(block_tables, "block_tables"), block_tables.shape[1],
+                                _dev_or_pinned(context_lens, "context_lens"), int(max_context_len), float(scale),
                                 int(partition_size), _dev(workspace, "workspace"),
                                 workspace.numel() * workspace.element_size(), _stream(stream)),
            "pkv_paged_decode")
@@ -247,15 +248,17 @@ def pkv_paged_decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Ten
                             context_lens: torch.Tensor, max_context_len: int, scale: float, partition_size: int,
                             workspace: torch.Tensor, stream=None) -> None:
     """Writes each sequence's new K/V row (k_new, v_new: [num_seqs, num_kv_heads, head_dim], q's dtype)
-    at position context_lens[i] - 1, then decodes as pkv_paged_decode."""
+    at position context_lens[i] - 1, then decodes as pkv_paged_decode.  out, q, k_new, v_new,
+    block_tables and context_lens may be pinned host memory (read and written in place)."""
     assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
     assert k_new.dtype == q.dtype and v_new.dtype == q.dtype and k_new.shape == v_new.shape
     assert k_new.shape[0] == q.shape[0] and k_new.is_contiguous() and v_new.is_contiguous()
-    _check(lib.pkv_paged_decode_append(_dev(out, "out"), _dev(q, "q"), pkv_dtype_of(q), q.shape[0], q.shape[1],
-                                       _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+    _check(lib.pkv_paged_decode_append(_dev_or_pinned(out, "out"), _dev_or_pinned(q, "q"), pkv_dtype_of(q),
+                                       q.shape[0], q.shape[1], _dev_or_pinned(k_new, "k_new"),
+                                       _dev_or_pinned(v_new, "v_new"), _dev(k_cache, "k_cache"),
                                        _dev(v_cache, "v_cache"), ctypes.byref(desc),
-                                       _dev(block_tables, "block_tables"), block_tables.shape[1],
-                                       _dev(context_lens, "context_lens"), int(max_context_len), float(scale),
+                                       _dev_or_pinned(block_tables, "block_tables"), block_tables.shape[1],
+                                       _dev_or_pinned(context_lens, "context_lens"), int(max_context_len), float(scale),
                                        int(partition_size), _dev(workspace, "workspace"),
                                        workspace.numel() * workspace.element_size(), _stream(stream)),
            "pkv_paged_decode_append")

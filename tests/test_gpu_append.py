@@ -139,3 +139,40 @@ def test_clamped_length_writes_nothing_and_is_flagged():
     assert torch.equal(kc[blk, :, off], case.k_new[0].to(dev))
     assert all(int(b) == blk and int(o) == off for b, _, o, _ in ch.tolist())
     assert torch.equal((vc != v0).nonzero()[:, [0, 2]].unique(dim=0).cpu(), torch.tensor([[blk, off]]))
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_pinned_host_inputs_and_output_match_device_ones(fused):
+    """out, q, new K/V, tables and lengths in pinned host memory are read and written in
+    place by the kernels; results are bit-identical to device-resident buffers."""
+    import paged_kv_cache_160_gb300 as pkv
+    case = synth.make_decode_case("pinned", 193, [1, 15, 16, 17, 300, 1000], 28, 4, 128, "bf16", "bf16")
+    plan = product_plan(case)
+    dev = torch.device("cuda")
+    max_len = max(plan.lens)
+    ws = torch.zeros(pkv.pkv_decode_workspace_bytes(case.num_seqs, 28, 4, 128, 16, max_len, 0), dtype=torch.uint8,
+                     device=dev)
+    tables = torch.tensor(plan.tables, dtype=torch.int32)
+    lens = torch.tensor(plan.lens, dtype=torch.int32)
+    results = []
+    for where in ("device", "pinned"):
+        kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+        desc = pkv.cache_desc(kc)
+        if where == "device":
+            q, tb, ln, kn, vn = case.q.to(dev), tables.to(dev), lens.to(dev), case.k_new.to(dev), case.v_new.to(dev)
+            out = torch.empty(case.q.shape, dtype=case.q.dtype, device=dev)
+        else:
+            q, tb, ln = case.q.clone().pin_memory(), tables.clone().pin_memory(), lens.clone().pin_memory()
+            kn, vn = case.k_new.clone().pin_memory(), case.v_new.clone().pin_memory()
+            out = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
+        if fused:
+            pkv.pkv_paged_decode_append(out, q, kn, vn, kc, vc, desc, tb, ln, max_len, case.scale, 0, ws)
+        else:
+            pkv.pkv_paged_decode(out, q, kc, vc, desc, tb, ln, max_len, case.scale, 0, ws)
+        torch.cuda.synchronize()
+        results.append((out.cpu(), kc.cpu(), vc.cpu()))
+    assert pkv.pkv_get_device_error() == 0
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.isfinite(results[0][0].float()).all()
+    assert np.array_equal(codes(results[0][1]), codes(results[1][1]))
+    assert np.array_equal(codes(results[0][2]), codes(results[1][2]))
