@@ -531,6 +531,7 @@ def run_gpu(args):
                                                 "host_to_device": round(sw_link[1], 1)}},
         "cache_ops": cache_ops,
         "host_plan_us": round(host_plan_us, 1),
+        "host_step": host_step_measure(case) if case.writes else None,
         "gpu_launches": (3 if case.writes and not fused else 2) * K,   # (kv_write,) decode, merge per step
         "unfused_step": None if unfused_ms is None else {
             "ms_per_step": round(unfused_ms, 5), "value": round(aggregate_gbs(step_bytes, unfused_ms, 1), 1),
@@ -543,6 +544,32 @@ def run_gpu(args):
     if ws_n > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def host_step_measure(case, n_steps: int = 20) -> dict:
+    """The native block-manager step (pkv_bm_step_decode: one slot per sequence, copy-on-write
+    pairs, exported tables and lengths) on the workload's pool, timed over n_steps consecutive
+    steps after an untimed set-up."""
+    import ctypes
+    from paged_kv_cache_160_gb300 import BlockManager
+    from paged_kv_cache_160_gb300._binding import lib
+    from tests.harness import _import_all, max_blocks_of
+    bm = BlockManager(case.num_blocks, case.block_size)
+    _import_all(bm, case)
+    n = case.num_seqs
+    mb = max_blocks_of(case) + -(-n_steps // case.block_size) + 1
+    seqs = (ctypes.c_int64 * n)(*range(n))
+    slots = (ctypes.c_int64 * n)()
+    pairs = (ctypes.c_int32 * (2 * n))()
+    tables = (ctypes.c_int32 * (n * mb))()
+    lens = (ctypes.c_int32 * n)()
+    nc = ctypes.c_int()
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        assert lib.pkv_bm_step_decode(bm._h, seqs, n, mb, slots, pairs, ctypes.byref(nc), tables, lens) == 0
+    dt = (time.perf_counter() - t0) / n_steps
+    return {"us_per_step": round(dt * 1e6, 2), "seqs": n, "steps": n_steps,
+            "what": "pkv_bm_step_decode through ctypes: append one slot per sequence, export tables and lengths"}
 
 
 def cache_ops_measure(pkv, case, plan, kc, vc, desc, k_new, v_new, slots, write_bytes, stream,
