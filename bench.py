@@ -65,7 +65,7 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture each), valid only for the
 # kernel source with this hash; when the source changes, traffic is reported as null until
 # re-measured.
-TRAFFIC = {"source_sha1": "bd8f055ea42932ee06ecf674fc122281dd99d3b8", "bytes_per_launch": 161774592}
+TRAFFIC = {"source_sha1": "aabb1d5dca5ecc7a6f5daf1ee59b2bd12bc1de7c", "bytes_per_launch": 161774592}
 
 
 def _src_hash() -> str:

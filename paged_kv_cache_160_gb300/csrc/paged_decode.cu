@@ -27,9 +27,14 @@
 //     the fragments are loaded with plain shared loads in a head_dim/token order chosen so
 //     every lane reads 16 contiguous bytes, and converted exactly to fp16.
 //   * A range that covers only part of a (sequence, kv head) writes a partial (m, l, o) to
-//     the workspace (at most two per worker); the last arriving piece (atomic counter, no
-//     waiting) merges all pieces by log-sum-exp and resets the counter, so one launch does
-//     split + merge.
+//     the workspace (at most two per worker) and the worker holding the segment's first
+//     tile describes its pieces; a second kernel, launched as a programmatic dependent,
+//     merges them by log-sum-exp.  A segment that lies inside one range is written directly.
+//   * Everything that depends only on lengths and block tables (prefix sums, ranges,
+//     cursors, first block ids, the pool rows of the first tiles) runs before the wait on
+//     the previous kernel, in 32-bit arithmetic; after it only the TMA issues remain.
+//   * Fused append (pkv_paged_decode_append): the warp holding a segment's last tile also
+//     places the step's new K/V row there, in the staged tile and in the cache.
 #include <algorithm>
 #include <utility>
 
