@@ -176,3 +176,13 @@ def test_pinned_host_inputs_and_output_match_device_ones(fused):
     assert torch.isfinite(results[0][0].float()).all()
     assert np.array_equal(codes(results[0][1]), codes(results[1][1]))
     assert np.array_equal(codes(results[0][2]), codes(results[1][2]))
+
+
+def test_very_large_batch_takes_the_four_warp_layout():
+    """4500 sequences (the four-warp layout): fused and unfused agree exactly; sampled rows
+    match the oracle."""
+    rng = np.random.default_rng(16)
+    lens = [int(x) for x in rng.integers(1, 40, size=4500)]
+    case = synth.make_decode_case("huge_batch_fused", 182, lens, 4, 1, 128, "bf16", "bf16")
+    rows = sorted({(int(s), int(h)) for s, h in zip(rng.integers(0, 4500, 300), rng.integers(0, 4, 300))})
+    _check_fused(case, decode_rows=rows)
