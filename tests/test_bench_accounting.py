@@ -1,0 +1,44 @@
+"""The bench's algorithmic-byte accounting (the roofline's numerator), pinned to closed forms.
+
+Decode bytes = every unique attended K/V row once (K and V) + q and out + one table entry per
+16-token tile + one length per sequence; write bytes = the new rows read and written + their
+slots.  A prefix shared through identical block ids is counted once.
+"""
+import bench
+import synth
+from tests.harness import product_plan
+
+
+def _closed_form(lens_after, S, Hq, Hkv, D, elt, shared_rows, T):
+    rows = sum(lens_after) - shared_rows
+    tiles = sum(-(-L // 16) for L in lens_after)
+    decode = 2 * rows * Hkv * D * elt + 2 * S * Hq * D * 2 + 4 * tiles + 4 * S
+    write = 2 * 2 * T * Hkv * D * elt + 8 * T
+    return decode, write
+
+
+def test_private_blocks_count_every_row():
+    lens = [1, 15, 16, 17, 200]
+    case = synth.make_decode_case("acct_private", 11, lens, 8, 2, 64, "f16", "f16")
+    plan = product_plan(case)
+    after = [L + 1 for L in lens]
+    assert plan.lens == after
+    assert bench.workload_bytes(case, plan) == (*_closed_form(after, 5, 8, 2, 64, 2, 0, 5), sum(after))
+
+
+def test_a_shared_prefix_is_counted_once():
+    # sequences 1..4 reuse sequence 0's first two (full) blocks: 4 x 32 rows are not re-counted
+    lens = [40, 50, 60, 70, 80]
+    case = synth.make_decode_case("acct_shared", 5, lens, 8, 2, 64, "f16", "f16",
+                                  share={i: (0, 2) for i in range(1, 5)})
+    plan = product_plan(case)
+    after = [L + 1 for L in lens]
+    assert bench.workload_bytes(case, plan) == (*_closed_form(after, 5, 8, 2, 64, 2, 4 * 32, 5), sum(after))
+
+
+def test_e4m3_rows_are_one_byte_and_no_write():
+    lens = [33, 100]
+    case = synth.make_decode_case("acct_e4m3", 12, lens, 32, 8, 128, "bf16", "e4m3", write=False)
+    plan = product_plan(case)
+    decode, write = _closed_form(lens, 2, 32, 8, 128, 1, 0, 0)
+    assert bench.workload_bytes(case, plan) == (decode, write, sum(lens))
