@@ -221,9 +221,11 @@ PKV_API pkv_status pkv_paged_decode_append(void* out, const void* q, pkv_dtype q
  * serving loop that may not call cudaMalloc on its hot path because cudaMalloc can
  * synchronise the whole device.  Same arguments and results as pkv_paged_decode, minus the
  * workspace: the library keeps one fixed scratch array of pkv_noalloc_scratch_bytes()
- * (24 MiB) on every device that loads it, resident until the process exits.  A call that
- * needs more scratch than that (per pkv_decode_workspace_bytes) returns PKV_ERR_WORKSPACE
- * and enqueues nothing.  No call allocates, frees or clears device memory: each call
+ * (24 MiB) on every device that loads it, resident until the process exits.  Arguments are
+ * checked exactly as pkv_paged_decode checks them, in the same order, so an invalid call
+ * returns the same status from both entry points.  A valid call that needs more scratch
+ * than the array holds (per pkv_decode_workspace_bytes) returns PKV_ERR_WORKSPACE and
+ * enqueues nothing.  No call allocates, frees or clears device memory: each call
  * rewrites the parts of the array it later reads, so leftovers of earlier calls do no
  * harm.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any

@@ -19,6 +19,9 @@ What it computes, and where the method is stated:
                          (Lecture 33 §2.4; "PagedAttention ... virtual memory" §3.3).
 * ``block_manager``    — free-block FIFO, ref_cnt, append/fork/CoW/free
                          ("PagedAttention ... virtual memory" §3.2–§3.3, Lecture 33 §2.4).
+* ``workload``         — the oracle's side of one synthetic step: planning on the model
+                         above, stored codes of the synthetic tensors, and the step's write
+                         and decode on a subset of its sequences.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against
 values the pages print, closed forms, library routines on contiguous inputs, or

@@ -865,22 +865,20 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
 }  // extern "C"
 
 namespace pkv {
-namespace {
 
-// Both decode entry points: plain (k_new == v_new == nullptr) or with the fused append.
-pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
-                       const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
-                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
-                       int max_context_len, float scale, int partition_size, void* workspace,
-                       size_t workspace_bytes, pkv_stream_t stream, const void* k_new, const void* v_new) {
+// The argument checks shared by every decode entry point.  On PKV_OK, *need holds the
+// workspace bytes the call needs (0 when num_seqs == 0: nothing to do).
+pkv_status decode_check(const void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                        const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                        int max_context_len, int partition_size, size_t* need) {
+  *need = 0;
   pkv_status st = check_cache_desc(cache);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq < 0 || max_context_len < 0 || partition_size < 0)
     return PKV_ERR_INVALID_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
-  if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
-    return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return PKV_ERR_INVALID_ARG;
@@ -903,10 +901,31 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs
     return PKV_ERR_UNSUPPORTED;
   const int grid = decode_grid();
   if (int64_t(grid) * kMaxWarps >= (int64_t(1) << 16)) return PKV_ERR_UNSUPPORTED;
+  *need = layout(num_seqs, cache->num_kv_heads, group, D, num_slots(grid * kMaxWarps)).total;
+  return PKV_OK;
+}
+
+namespace {
+
+// Both decode entry points: plain (k_new == v_new == nullptr) or with the fused append.
+pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                       const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                       const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                       int max_context_len, float scale, int partition_size, void* workspace,
+                       size_t workspace_bytes, pkv_stream_t stream, const void* k_new, const void* v_new) {
+  size_t need = 0;
+  pkv_status st = decode_check(out, q, q_dtype, num_seqs, num_heads, k_cache, v_cache, cache, block_tables,
+                               max_blocks_per_seq, context_lens, max_context_len, partition_size, &need);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+    return PKV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  const int group = num_heads / cache->num_kv_heads;
+  const int D = cache->head_dim;
+  const int64_t max_len = std::min<int64_t>(int64_t(max_blocks_per_seq) * cache->block_size, max_context_len);
+  const int grid = decode_grid();
   const int part_blocks = partition_size / kBS;
-  const int64_t slots = num_slots(grid * kMaxWarps);
-  const Layout lay = layout(num_seqs, cache->num_kv_heads, group, D, slots);
-  if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  const Layout lay = layout(num_seqs, cache->num_kv_heads, group, D, num_slots(grid * kMaxWarps));
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
 

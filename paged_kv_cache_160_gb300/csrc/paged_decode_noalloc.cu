@@ -47,13 +47,12 @@ pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype,
                                     const int32_t* block_tables, int max_blocks_per_seq,
                                     const int32_t* context_lens, int max_context_len, float scale,
                                     int partition_size, pkv_stream_t stream) {
-  pkv_status st = pkv::check_cache_desc(cache);
-  if (st != PKV_OK) return st;
-  if (num_seqs < 0 || num_heads <= 0) return PKV_ERR_INVALID_ARG;
-  if (num_seqs == 0) return PKV_OK;
-  const size_t need = pkv_decode_workspace_bytes(num_seqs, num_heads, cache->num_kv_heads, cache->head_dim,
-                                                 cache->block_size, max_context_len, partition_size);
-  if (need == 0) return PKV_ERR_INVALID_ARG;
+  // The same argument checks, in the same order, as pkv_paged_decode, so both calls give the
+  // same status for the same invalid arguments; only then is the scratch size compared.
+  size_t need = 0;
+  pkv_status st = pkv::decode_check(out, q, q_dtype, num_seqs, num_heads, k_cache, v_cache, cache, block_tables,
+                                    max_blocks_per_seq, context_lens, max_context_len, partition_size, &need);
+  if (st != PKV_OK || num_seqs == 0) return st;
   if (need > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;   // more than the fixed array holds
   void* scratch = scratch_on_current_device();
   if (!scratch) return PKV_ERR_CUDA;

@@ -37,6 +37,13 @@ inline int dtype_bytes(pkv_dtype d) { return d == PKV_FP8_E4M3 ? 1 : 2; }
 // Shared checks of a cache descriptor; returns PKV_OK or the failing status.
 pkv_status check_cache_desc(const pkv_cache_desc* c);
 
+// The argument checks of the paged-decode entry points (no CUDA work is enqueued).  On
+// PKV_OK, *need holds the workspace bytes the call needs (0 when num_seqs == 0).
+pkv_status decode_check(const void* out, const void* q, pkv_dtype q_dtype, int num_seqs, int num_heads,
+                        const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                        const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                        int max_context_len, int partition_size, size_t* need);
+
 #ifdef __CUDACC__
 // Launch with programmatic stream serialization: the kernel may be scheduled while the
 // previous kernel on the stream still runs, and must call griddep_wait() before it touches

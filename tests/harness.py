@@ -18,99 +18,25 @@ sequence).
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 from typing import Dict, List, Optional, Tuple
 
 import numpy as np
 import torch
 
+from oracle.workload import codes, q_f64  # noqa: F401  (re-exported for the tests)
+from paged_kv_cache_160_gb300.planner import (  # noqa: F401  (re-exported for the tests)
+    Plan, append_slots, import_all, max_blocks_of, product_plan)
+
 TOL = {"f16": 2e-3, "bf16": 1e-2, "e4m3": 3e-2}
-SCRATCH_SEQ = 1 << 40
-
-
-def codes(t: torch.Tensor) -> np.ndarray:
-    """Stored codes of a host tensor (uint16 for f16/bf16, uint8 for e4m3 bytes)."""
-    t = t.contiguous()
-    if t.dtype in (torch.float16, torch.bfloat16):
-        return t.view(torch.int16).numpy().view(np.uint16)
-    return t.view(torch.uint8).numpy()
-
-
-def q_f64(t: torch.Tensor) -> np.ndarray:
-    from oracle.formats import to_f64
-    return to_f64(codes(t), "bf16" if t.dtype == torch.bfloat16 else "f16")
-
-
-def max_blocks_of(case) -> int:
-    mb = max([-(-(L + 1) // case.block_size) for L in case.context_lens] + [1])
-    if case.chunk is not None:
-        mb = max(mb, -(-(case.chunk.prefix_len + case.chunk.q_len) // case.block_size))
-    return mb
-
-
-@dataclass
-class Plan:
-    tables: List[List[int]]
-    lens: List[int]
-    slots: List[int]
-    cows: List[Tuple[int, int]]
-    chunk_table: Optional[List[int]] = None
-    chunk_slots: List[int] = field(default_factory=list)
-    share_pairs: List[Tuple[int, int]] = field(default_factory=list)
-
-
-def _import_all(bm, case):
-    for i, (blocks, L) in enumerate(zip(case.seq_blocks, case.context_lens)):
-        bm.import_seq(i, blocks, L)
-    if case.chunk is not None:
-        bm.import_seq(case.num_seqs, case.chunk.blocks, case.chunk.prefix_len)
 
 
 def oracle_plan(case) -> Plan:
-    from oracle.block_manager import BlockManagerModel
-    bm = BlockManagerModel(case.num_blocks, case.block_size)
-    _import_all(bm, case)
-    mb = max_blocks_of(case)
-    slots, cows = [], []
-    if case.writes:
-        for i in range(case.num_seqs):
-            s, c = bm.append_slot(i)
-            slots.append(s)
-            if c is not None:
-                cows.append(c)
-    tables, lens = bm.export(list(range(case.num_seqs)), mb)
-    plan = Plan(tables, lens, slots, cows)
-    if case.chunk is not None:
-        plan.chunk_slots, ccows = bm.append_slots(case.num_seqs, case.chunk.q_len)
-        plan.cows += ccows
-        plan.chunk_table = bm.export([case.num_seqs], mb)[0][0]
-        if case.copy_pairs:
-            bm.allocate(SCRATCH_SEQ, case.copy_pairs * case.block_size)
-            plan.share_pairs = list(zip(plan.chunk_table[:case.copy_pairs], bm.tables[SCRATCH_SEQ]))
-    return plan
-
-
-def product_plan(case) -> Plan:
-    from paged_kv_cache_160_gb300 import BlockManager
-    bm = BlockManager(case.num_blocks, case.block_size)
-    _import_all(bm, case)
-    mb = max_blocks_of(case)
-    seqs = list(range(case.num_seqs))
-    if case.writes:
-        slots, cows, tables, lens = bm.step_decode(seqs, mb)
-    else:
-        slots, cows = [], []
-        tables, lens = bm.export(seqs, mb)
-    plan = Plan(tables, lens, slots, list(cows))
-    if case.chunk is not None:
-        plan.chunk_slots, ccows = bm.append_slots(case.num_seqs, case.chunk.q_len)
-        plan.cows += ccows
-        plan.chunk_table = bm.export([case.num_seqs], mb)[0][0]
-        if case.copy_pairs:
-            bm.allocate(SCRATCH_SEQ, case.copy_pairs * case.block_size)
-            tab = bm.export([SCRATCH_SEQ], case.copy_pairs)[0][0]
-            plan.share_pairs = list(zip(plan.chunk_table[:case.copy_pairs], tab))
-    return plan
+    """The same step planned on the oracle's block-manager model (oracle.workload)."""
+    from oracle.workload import plan_step
+    st = plan_step(case)
+    return Plan(st["tables"], st["lens"], st["slots"], st["cows"], st["chunk_table"], st["chunk_slots"],
+                st["share_pairs"])
 
 
 # ---------------------------------------------------------------------------------------
@@ -166,12 +92,6 @@ class DeviceResult:
     decode: torch.Tensor          # [S, Hq, D] host, q dtype
     prefill: Optional[torch.Tensor]
     device_error: int
-
-
-def append_slots(case, plan: Plan) -> List[int]:
-    """Slot of position L - 1 of each decode sequence (L = its length after the step)."""
-    bs = case.block_size
-    return [plan.tables[i][(L - 1) // bs] * bs + (L - 1) % bs if L >= 1 else -1 for i, L in enumerate(plan.lens)]
 
 
 def device_run(case, plan: Plan, partition_size: Optional[int] = None, keep_intermediate: bool = True,

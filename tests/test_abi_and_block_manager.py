@@ -75,6 +75,41 @@ def test_argument_checks_run_on_host_without_gpu():
     assert L.pkv_check_bounded_wait(2_000_000_000, None) == 1
 
 
+def test_noalloc_decode_returns_the_same_status_as_the_workspace_call():
+    """Invalid arguments give the same status from pkv_paged_decode_noalloc as from
+    pkv_paged_decode (both run the same host checks before anything else); nothing here
+    reaches the GPU."""
+    import paged_kv_cache_160_gb300 as pkv
+    from paged_kv_cache_160_gb300._binding import CacheDesc
+    L = pkv.lib
+    good = CacheDesc(64, 4, 16, 128, 1, None, None)
+    cases = [
+        # (description, out, q, q_dtype, num_seqs, num_heads, k, v, desc, tables, max_blocks, lens, max_len, part)
+        ("null out", None, 16, 1, 4, 8, 16, 16, good, 16, 8, 16, 128, 0),
+        ("null q", 16, None, 1, 4, 8, 16, 16, good, 16, 8, 16, 128, 0),
+        ("null lengths", 16, 16, 1, 4, 8, 16, 16, good, 16, 8, None, 128, 0),
+        ("misaligned k", 16, 16, 1, 4, 8, 24, 16, good, 16, 8, 16, 128, 0),
+        ("bad GQA split", 16, 16, 1, 4, 6, 16, 16, good, 16, 8, 16, 128, 0),
+        ("group above 8", 16, 16, 1, 4, 36, 16, 16, good, 16, 8, 16, 128, 0),
+        ("block size 8", 16, 16, 1, 4, 8, 16, 16, CacheDesc(64, 4, 8, 128, 1, None, None), 16, 8, 16, 128, 0),
+        ("head_dim 96", 16, 16, 1, 4, 8, 16, 16, CacheDesc(64, 4, 16, 96, 1, None, None), 16, 8, 16, 128, 0),
+        ("partition 24", 16, 16, 1, 4, 8, 16, 16, good, 16, 8, 16, 128, 24),
+        ("q dtype e4m3", 16, 16, 2, 4, 8, 16, 16, good, 16, 8, 16, 128, 0),
+        ("negative seqs", 16, 16, 1, -1, 8, 16, 16, good, 16, 8, 16, 128, 0),
+        ("no table columns", 16, 16, 1, 4, 8, 16, 16, good, 16, 0, 16, 128, 0),
+        ("e4m3 without scales", 16, 16, 1, 4, 8, 16, 16, CacheDesc(64, 4, 16, 128, 2, None, None), 16, 8, 16,
+         128, 0),
+        ("tile count past 2^31", 16, 16, 1, 65536, 8, 16, 16, good, 16, 8192, 16, 131072, 0),
+        ("nothing to do", 16, 16, 1, 0, 8, 16, 16, good, 16, 8, 16, 128, 0),
+    ]
+    for name, out, q, qd, S, H, k, v, d, tb, mb, ln, ml, part in cases:
+        a = L.pkv_paged_decode(out, q, qd, S, H, k, v, ctypes.byref(d), tb, mb, ln, ml, 0.1, part, 16, 1 << 30,
+                               None)
+        b = L.pkv_paged_decode_noalloc(out, q, qd, S, H, k, v, ctypes.byref(d), tb, mb, ln, ml, 0.1, part, None)
+        assert a == b, (name, a, b)
+        assert (a == 0) == (name == "nothing to do"), (name, a)
+
+
 # ---------------------------------------------------------------------------------------
 # block manager: pins and parity with the oracle model
 # ---------------------------------------------------------------------------------------
