@@ -1,36 +1,46 @@
-"""Benchmark of the paged-KV decode step on GB300: effective HBM GB/s and seq-tokens/s.
+"""Benchmark of the paged-KV decode step on one GB300: effective HBM GB/s and seq-tokens/s.
 
-Workload: the Qwen2.5-7B-shaped GQA decode batch — 64 running sequences with context
-lengths uniform in [128, 2048], 28 query heads / 4 kv heads, head_dim 128, bf16 Q/K/V,
-16-token blocks in a shuffled pool ([num_blocks, 4, 16, 128], pool = blocks needed + 10%).
-One step = plan the step on the host block manager (done once; its cost is reported
-separately), the write of the 64 new tokens' K/V, then paged_decode over every sequence's
-L + 1 tokens.  Every new token belongs at its sequence's last position, so the write is
-fused into the decode call (pkv_paged_decode_append: two launches, the split-KV decode and
-the log-sum-exp merge of split segments as its programmatic dependent); kv_write + decode
-is timed beside it.
+Headline workload: the Qwen2.5-7B-shaped GQA decode batch — 64 running sequences with
+context lengths uniform in [128, 2048], 28 query heads / 4 kv heads, head_dim 128, bf16
+Q/K/V, 16-token blocks in a shuffled pool ([num_blocks, 4, 16, 128], pool = blocks needed +
+10%).  One step = the write of the 64 new tokens' K/V, then paged_decode over every
+sequence's L + 1 tokens.  Every new token belongs at its sequence's last position, so the
+write is fused into the decode call (pkv_paged_decode_append: two launches, the split-KV
+decode and the log-sum-exp merge of split segments as its programmatic dependent);
+kv_write + decode is timed beside it.  The step is planned once on the native block manager
+(its cost is reported separately).
 
-Timing: CUDA events on the launching stream.  The K timed steps are captured into one
-CUDA graph and replayed once between two events.  The decode call's own average duration
-(decode + merge, for its roofline) comes from a second graph of K calls timed the same way.
-Every step uses the next of R pool copies whose combined size is above 3x the L2 size, so
-no step finds its K/V in L2.  `value` is device-resident throughput.  `e2e` passes HOST
-buffers to the call: every step's inputs (q, new K/V, tables, lengths) are read in place
-from pinned host memory and its output is written to pinned host memory by the kernels,
-across NVLink-C2C.  The same steps with explicit staged H2D/D2H copies on copy streams are
-reported beside it.
+Timing: CUDA events on the launching stream around one CUDA graph of K steps.  Every step
+uses the next of R pool copies whose combined size is above 3x the L2 size, so no step
+finds its K/V in L2.  `value` is device-resident throughput.  `e2e` passes HOST buffers to
+the call: every step's inputs (q, new K/V, tables, lengths) are read in place from pinned
+host memory and its output is written to pinned host memory by the kernels, across
+NVLink-C2C; the same steps with staged H2D/D2H copies on copy streams are reported beside it.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload 2|3|4|5]
+The same line also reports, each timed the same way:
+  roofline.copy_same_size_gbs  a plain device copy moving the decode call's bytes (half read,
+                               half written), rotating over the same number of buffers;
+  workloads                    the decode call on the 13B MHA batch and the long-context
+                               e4m3 batch;
+  mixed_step                   the mixed chunked-prefill + decode step as one graph per step:
+                               kv_write of 640 tokens, the 512-row prefill chunk, paged_decode
+                               of 128 sequences, then copy_blocks of 64 pairs;
+  prefill_chunk, cache_ops, swap_blocks, host_step: single calls;
+  cpu_baseline                 the float64 oracle on the host cores, one core and all cores.
 
---workload picks another decode workload (3: 13B MHA, 4: long-context e4m3, 5: the mixed
-step's decode part); the default, 2, is the headline.
+    python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl reference] [--workload 2|3|4|5]
+
+--workload picks another decode workload for the headline fields (3: 13B MHA, 4: long-context
+e4m3, 5: the mixed step's decode part); the default, 2, is the headline.  The library runs on
+one GPU: --gpus N > 1 (or a torchrun launch with more than one rank) prints a one-line refusal.
 """
 from __future__ import annotations
 
 import os
 
-# The CPU baseline times the oracle with one BLAS thread; pin numpy's BLAS before it loads.
-for _var in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+# The CPU baseline times the oracle with one BLAS thread per process; pin numpy's BLAS
+# before it loads (spawned worker processes re-run this module's top level).
+for _var in ("OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS", "OMP_NUM_THREADS"):
     os.environ.setdefault(_var, "1")
 
 import argparse
@@ -60,12 +70,14 @@ WORKLOADS = {
 }
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM bytes per decode call on this workload (paged_decode_kernel + split_kv_merge_kernel,
-# dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture each), valid only for the
-# kernel source with this hash; when the source changes, traffic is reported as null until
-# re-measured.
-TRAFFIC = {"source_sha1": "aabb1d5dca5ecc7a6f5daf1ee59b2bd12bc1de7c", "bytes_per_launch": 161774592}
+# DRAM bytes per decode call on the headline workload (paged_decode_kernel +
+# split_kv_merge_kernel, dram__bytes_read.sum + dram__bytes_write.sum, mean of the two calls
+# of one ncu capture; ncu flushes the caches before each kernel, so the merge's reads of the
+# partials count as DRAM reads), valid only for the kernel source with this hash; when the
+# source changes, traffic is reported as null until re-measured.
+TRAFFIC = {"source_sha1": "d8283e5a4472d6a78c096af9d68140d151819d58", "bytes_per_launch": 159987840}
 
 
 def _src_hash() -> str:
@@ -83,35 +95,29 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def _bf16_peak() -> float:
+def _bf16_peak():
     """Measured dense bf16 TFLOP/s (burst: the prefill kernel is timed alone)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
-        return float(json.load(open(path))["bf16_tflops"])
-    return 1900.0
+        return float(json.load(open(path))["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def max_over_ranks(x: float, device) -> float:
-    """The largest value of x over all ranks (the slowest rank defines the timed region)."""
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
-        return x
-    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+def _world():
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
 
 
-def aggregate_gbs(bytes_per_rank: int, ms_per_step: float, world: int) -> float:
-    """Whole-job GB/s: every rank runs its own replica of the step (weak scaling)."""
-    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
-
-
-def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+def refuse_multi_gpu(args) -> bool:
+    """The library and its benchmark run on one GPU.  Under --gpus N > 1 or a multi-rank
+    launch, rank 0 prints one refusal line; every rank exits without GPU work."""
+    world, rank = _world()
+    if args.gpus == 1 and world == 1:
+        return False
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "impl": args.impl, "n_gpus": max(args.gpus, world),
+                          "unavailable": "single-GPU library: the decode path runs on one GPU and has no "
+                                         "multi-GPU mode; run with --gpus 1"}))
+    return True
 
 
 class ClockSampler:
@@ -167,38 +173,115 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
+# ---------------------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------------------
+
 def workload_bytes(case, plan):
-    """Algorithmic bytes of one step (each unique attended K/V row once)."""
-    Hkv, D, Hq = case.num_kv_heads, case.head_dim, case.num_heads
+    """Algorithmic bytes of one decode step: each unique attended K/V row once (K and V), q
+    and out, one table entry per 16-token tile and one length per sequence; and the step's
+    write (new rows read and written, plus their slots).  Returns (decode, write, tokens)."""
+    Hkv, D, Hq, bs = case.num_kv_heads, case.head_dim, case.num_heads, case.block_size
     kv_elt = 1 if case.kv_dtype == "e4m3" else 2
     q_elt = 2
     unique_rows = set()
     for t, L in zip(plan.tables, plan.lens):
         for j in range(L):
-            unique_rows.add(t[j // 16] * 16 + j % 16)
+            unique_rows.add(t[j // bs] * bs + j % bs)
     n_rows = len(unique_rows)
-    nblocks = sum(-(-L // 16) for L in plan.lens)
+    ntiles = sum(-(-L // 16) for L in plan.lens)
     S = case.num_seqs
-    decode = 2 * n_rows * Hkv * D * kv_elt + 2 * S * Hq * D * q_elt + 4 * nblocks + 4 * S
+    decode = 2 * n_rows * Hkv * D * kv_elt + 2 * S * Hq * D * q_elt + 4 * ntiles + 4 * S
     T = len(plan.slots)
     write = 2 * 2 * T * Hkv * D * kv_elt + 8 * T
     return decode, write, sum(plan.lens)
 
 
+def prefill_work(case, plan):
+    """The mixed step's prefill chunk: FLOPs = 4 * head_dim * (attended query-key pairs) * heads;
+    bytes = the chunk sequence's K/V rows once, its q and out, its table row."""
+    ch = case.chunk
+    Hkv, D, Hq = case.num_kv_heads, case.head_dim, case.num_heads
+    pairs = sum(ch.prefix_len + r + 1 for r in range(ch.q_len))
+    flops = 4 * D * pairs * Hq
+    rows = ch.prefix_len + ch.q_len
+    nbytes = 2 * rows * Hkv * D * 2 + 2 * ch.q_len * Hq * D * 2 + 4 * len(plan.chunk_table)
+    return flops, nbytes
+
+
+def mixed_step_work(case, plan):
+    """Bytes and FLOPs of the whole mixed step: the kv_write of every new row (decode tokens
+    and chunk rows), the decode attention, the prefill chunk and the copy-on-write pairs."""
+    Hkv, D = case.num_kv_heads, case.head_dim
+    decode, _, tokens = workload_bytes(case, plan)
+    T = len(plan.slots) + len(plan.chunk_slots)
+    write = 2 * 2 * T * Hkv * D * 2 + 8 * T
+    pf_flops, pf_bytes = prefill_work(case, plan)
+    block_bytes = Hkv * case.block_size * D * 2
+    copy = 2 * 2 * len(plan.share_pairs) * block_bytes + 8 * len(plan.share_pairs)
+    dec_flops = 4 * D * tokens * case.num_heads
+    return {"decode_bytes": decode, "write_bytes": write, "prefill_bytes": pf_bytes, "copy_bytes": copy,
+            "bytes": decode + write + pf_bytes + copy, "prefill_flops": pf_flops, "decode_flops": dec_flops,
+            "flops": pf_flops + dec_flops, "tokens": tokens}
+
+
+# ---------------------------------------------------------------------------------------
+# timing helpers
+# ---------------------------------------------------------------------------------------
+
+def graph_ms(stream, fn, n_calls: int, warm_calls: int) -> float:
+    """Average ms per call of fn(k) for k = 0..n_calls-1, captured as one CUDA graph and
+    replayed between two events.  Before that: warm_calls eager calls (the library's
+    per-device state exists before capture) and one untimed replay of the same graph (a
+    graph's first launch also uploads it to the device)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for k in range(max(2, warm_calls)):
+            fn(k)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for k in range(n_calls):
+            fn(warm_calls + k)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / n_calls
+
+
+def rotation(case, l2: int) -> int:
+    """Pool copies to rotate over so that their combined size exceeds 3x L2."""
+    pool_bytes = 2 * case.k_cache.numel() * case.k_cache.element_size()
+    return max(1, math.ceil(3 * l2 / pool_bytes) + 1) if pool_bytes < 3 * l2 else 1
+
+
+def device_case(pkv, case, dev, R):
+    import torch
+    kcs = [case.k_cache.to(dev) for _ in range(R)]
+    vcs = [case.v_cache.to(dev) for _ in range(R)]
+    ks = case.k_scale.to(dev) if case.k_scale is not None else None   # e4m3 caches: per-head scales
+    vs = case.v_scale.to(dev) if case.v_scale is not None else None
+    descs = [pkv.cache_desc(k, ks, vs) for k in kcs]
+    return kcs, vcs, descs
+
+
+# ---------------------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------------------
+
 def run_gpu(args):
-    import numpy as np
     import torch
 
     import paged_kv_cache_160_gb300 as pkv
     import synth
-    from tests.harness import append_slots, product_plan
+    from paged_kv_cache_160_gb300.planner import append_slots, product_plan
 
-    ws_n, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws_n > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
 
     case = synth.CONFIG_BUILDERS[args.workload]()
     t0 = time.perf_counter()
@@ -211,11 +294,7 @@ def run_gpu(args):
     l2 = getattr(props, "L2_cache_size", 0) or 132 * 1024 * 1024
     pool_bytes = 2 * case.k_cache.numel() * case.k_cache.element_size()
     R = max(2, math.ceil(3 * l2 / pool_bytes) + 1)
-    kcs = [case.k_cache.to(dev) for _ in range(R)]
-    vcs = [case.v_cache.to(dev) for _ in range(R)]
-    k_scale = case.k_scale.to(dev) if case.k_scale is not None else None   # e4m3 caches: per-head scales
-    v_scale = case.v_scale.to(dev) if case.v_scale is not None else None
-    descs = [pkv.cache_desc(k, k_scale, v_scale) for k in kcs]
+    kcs, vcs, descs = device_case(pkv, case, dev, R)
     q = case.q.to(dev)
     k_new = case.k_new.to(dev) if case.writes else None
     v_new = case.v_new.to(dev) if case.writes else None
@@ -225,8 +304,8 @@ def run_gpu(args):
     out = torch.empty_like(q)
     max_len = max(plan.lens)
     part = case.partition_size
-    wsb = pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim, 16,
-                                         max_len, part)
+    wsb = pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads, case.head_dim,
+                                         case.block_size, max_len, part)
     ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -236,15 +315,15 @@ def run_gpu(args):
 
     def write(r):
         if case.writes:
-            pkv.pkv_kv_write(k_new, v_new, slots, kcs[r], vcs[r], descs[r])
+            pkv.pkv_kv_write(k_new, v_new, slots, kcs[r], vcs[r], descs[r], stream)
 
     def decode(r):
-        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, part, ws)
+        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, part, ws, stream)
 
     def step(r, fuse=fused):
         if fuse:
             pkv.pkv_paged_decode_append(out, q, k_new, v_new, kcs[r], vcs[r], descs[r], tables, lens, max_len,
-                                        case.scale, part, ws)
+                                        case.scale, part, ws, stream)
         else:
             write(r)
             decode(r)
@@ -258,16 +337,9 @@ def run_gpu(args):
     assert pkv.pkv_get_device_error(stream) == 0
     K, W = args.steps, args.warmup
 
-    def barrier():
-        if ws_n > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     # The timed loop is one CUDA graph of K steps (each: the fused append + decode -> split-KV
     # merge, or kv_write -> decode -> merge, launched as programmatic dependents), rotating over
-    # the pool copies.  The decode kernel's own average duration (decode + merge, without the
-    # write, for its roofline) is timed the same way on a graph of K decodes alone; event nodes
-    # between kernels would break the programmatic launches and inflate it.
+    # the pool copies.
     def capture(n_steps, first, kind="step"):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
@@ -283,52 +355,54 @@ def run_gpu(args):
 
     g_warm = capture(W, 0)
     g_timed = capture(K, W)
-    g_dec_warm = capture(W, 0, kind="step" if fused else "decode")   # the step's decode call alone
-    g_dec = capture(K, W, kind="step" if fused else "decode")
     g_unf = capture(K, W, kind="unfused") if fused else None
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
+    # W warm-up steps, then one untimed replay of the timed graph itself (a graph's first
+    # launch also uploads it to the device), then the timed replay.
     with torch.cuda.stream(stream):
         g_warm.replay()
+        g_timed.replay()
     stream.synchronize()
-    barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with ClockSampler(0) as clk:
         with torch.cuda.stream(stream):
             start.record(stream)
             g_timed.replay()
             end.record(stream)
         stream.synchronize()
-        barrier()
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            g_dec_warm.replay()
-            d_start.record(stream)
-            g_dec.replay()
-            d_end.record(stream)
-        stream.synchronize()
+        # The decode call alone, for its roofline: the step's call when the write is fused
+        # (it is the whole step), else decode + merge without the write.
+        if fused:
+            dec_avg_ms = None
+        else:
+            dec_avg_ms = graph_ms(stream, lambda k: decode(k % R), K, W)
         unfused_ms = None
         if g_unf is not None:
             u_start, u_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
-                g_warm.replay()
+                g_unf.replay()
                 u_start.record(stream)
                 g_unf.replay()
                 u_end.record(stream)
             stream.synchronize()
             unfused_ms = u_start.elapsed_time(u_end) / K
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), dev)
-    dec_avg_ms = d_start.elapsed_time(d_end) / K
+    elapsed_ms = start.elapsed_time(end)
+    if dec_avg_ms is None:
+        dec_avg_ms = elapsed_ms / K
     assert pkv.pkv_get_device_error(stream) == 0
 
+    # The same-size ceiling: a plain device copy moving the decode call's bytes (half read,
+    # half written), rotating over R buffer pairs, one graph of K copies.
+    roof_bytes = step_bytes if fused else decode_bytes        # the fused call also moves the new rows
+    half = (roof_bytes // 2) & ~4095                          # whole 4 KiB pages: the copy's fast path
+    src = [torch.empty(half, dtype=torch.uint8, device=dev).fill_(1) for _ in range(R)]
+    dst = [torch.empty(half, dtype=torch.uint8, device=dev) for _ in range(R)]
+    copy_ms = graph_ms(stream, lambda k: dst[k % R].copy_(src[k % R]), K, W)
+    copy_gbs = 2 * half / (copy_ms * 1e-3) / 1e9
+    del src, dst
+
     # ---- end to end, staged: explicit copies on copy streams --------------------------------
-    # A serving loop's shape: each step's inputs (q, new K/V, slots, tables, lengths) sit in one
-    # pinned staging buffer and go up in one copy; device inputs and outputs are double-
-    # buffered; uploads run on one copy stream and output downloads on another, ordered by
-    # events, so step k+1's upload and step k's download overlap step k's kernels.  Every step
-    # still moves its full input and output bytes across the host link.
     host_parts = [case.q, torch.tensor(plan.tables, dtype=torch.int32), torch.tensor(plan.lens, dtype=torch.int32)]
     if case.writes:
         host_parts += [case.k_new, case.v_new]
@@ -379,13 +453,13 @@ def run_gpu(args):
                 if fused:
                     kni, vni = dv[i][3:5]
                     pkv.pkv_paged_decode_append(outs[i], qi, kni, vni, kcs[r], vcs[r], descs[r], tbi, lni, max_len,
-                                                case.scale, part, ws)
+                                                case.scale, part, ws, stream)
                 else:
                     if case.writes:
                         kni, vni, sli = dv[i][3:]
-                        pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r])
+                        pkv.pkv_kv_write(kni, vni, sli, kcs[r], vcs[r], descs[r], stream)
                     pkv.pkv_paged_decode(outs[i], qi, kcs[r], vcs[r], descs[r], tbi, lni, max_len, case.scale,
-                                         part, ws)
+                                         part, ws, stream)
                 step_done.record(stream)
                 down.wait_event(step_done)
                 with torch.cuda.stream(down):
@@ -402,16 +476,15 @@ def run_gpu(args):
     g_e2e_warm = e2e_graph(W, 0)
     g_e2e = e2e_graph(K, W)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         g_e2e_warm.replay()
+        g_e2e.replay()
         e_start.record(stream)
         g_e2e.replay()
         e_end.record(stream)
     stream.synchronize()
-    barrier()
-    staged_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
+    staged_ms = e_start.elapsed_time(e_end)
     for i in range(2):
         assert torch.equal(h_outs[i], out.cpu())
 
@@ -431,52 +504,49 @@ def run_gpu(args):
                 hs["kn"], hs["vn"] = case.k_new.clone().pin_memory(), case.v_new.clone().pin_memory()
             hsets.append(hs)
 
-        def zc_graph(n_steps, first):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-                for k in range(n_steps):
-                    hs, r = hsets[k % 2], (first + k) % R
-                    if fused:
-                        pkv.pkv_paged_decode_append(hs["out"], hs["q"], hs["kn"], hs["vn"], kcs[r], vcs[r], descs[r],
-                                                    hs["tb"], hs["ln"], max_len, case.scale, part, ws)
-                    else:
-                        pkv.pkv_paged_decode(hs["out"], hs["q"], kcs[r], vcs[r], descs[r], hs["tb"], hs["ln"],
-                                             max_len, case.scale, part, ws)
-            return g
+        def zc_call(k):
+            hs, r = hsets[k % 2], k % R
+            if fused:
+                pkv.pkv_paged_decode_append(hs["out"], hs["q"], hs["kn"], hs["vn"], kcs[r], vcs[r], descs[r],
+                                            hs["tb"], hs["ln"], max_len, case.scale, part, ws, stream)
+            else:
+                pkv.pkv_paged_decode(hs["out"], hs["q"], kcs[r], vcs[r], descs[r], hs["tb"], hs["ln"],
+                                     max_len, case.scale, part, ws, stream)
 
-        gz_warm, gz = zc_graph(W, 0), zc_graph(K, W)
-        z_start, z_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            gz_warm.replay()
-            z_start.record(stream)
-            gz.replay()
-            z_end.record(stream)
-        stream.synchronize()
-        barrier()
-        e2e_ms = max_over_ranks(z_start.elapsed_time(z_end), dev)
+        e2e_ms = graph_ms(stream, zc_call, K, W) * K
         for hs in hsets:
             assert torch.equal(hs["out"], out.cpu())
     else:
         e2e_ms = staged_ms
+    del d_in, outs, h_outs
     pf_ms, pf_flops = prefill_measure(dev)
     cache_ops = cache_ops_measure(pkv, case, plan, kcs[0], vcs[0], descs[0], k_new, v_new, slots, write_bytes,
                                   stream) if case.writes else None
     sw_out, sw_in, sw_bytes, sw_link = swap_measure(dev)
+    host_step = host_step_measure(case) if case.writes else None
+    del kcs, vcs, descs
+    torch.cuda.empty_cache()
 
     peak, peak_kind = _peaks()
+    bf16_peak, bf16_kind = _bf16_peak()
+    others = {}
+    mixed = None
+    if args.workload == 2 and not args.headline_only:
+        for n in (3, 4):
+            others[str(n)] = decode_call_measure(n, dev, l2, stream, peak, K, W)
+        mixed = mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak)
+
     ms_per_step = elapsed_ms / K
-    value = aggregate_gbs(step_bytes, ms_per_step, ws_n)
-    roof_bytes = step_bytes if fused else decode_bytes        # the fused call also moves the new rows
+    value = step_bytes / (ms_per_step * 1e-3) / 1e9
     achieved = roof_bytes / (dec_avg_ms * 1e-3) / 1e9
     traffic = (TRAFFIC["bytes_per_launch"] if args.workload == 2 and TRAFFIC["source_sha1"] == _src_hash()
                else None)
+    launches_per_step = 3 if case.writes and not fused else 2      # (kv_write,) decode, merge
     line = {
         "metric": METRIC,
         "value": round(value, 1),
         "unit": "GB/s",
-        "n_gpus": ws_n,
+        "n_gpus": 1,
         "steps": K,
         "warmup": W,
         "ms_per_step": round(ms_per_step, 5),
@@ -496,18 +566,26 @@ def run_gpu(args):
                                 ("pkv_kv_write + pkv_paged_decode + merge" if case.writes else
                                  "pkv_paged_decode + merge"),
                    "partition_size": part,
-                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
-        "seq_tokens_per_s": round(ws_n * tokens / (ms_per_step * 1e-3), 1),
-        "pct_of_nominal_8tbs": round(100 * value / ws_n / NOMINAL_HBM_GBS, 2),
-        "pct_of_measured_copy": round(100 * value / ws_n / peak, 2),
+                   "untimed_graph_replays": "the timed K-step graph is replayed once untimed after the W warm-up "
+                                            "steps (a graph's first launch also uploads it)",
+                   "parallelism": "single GPU"},
+        "seq_tokens_per_s": round(tokens / (ms_per_step * 1e-3), 1),
+        "pct_of_nominal_8tbs": round(100 * value / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_copy": round(100 * value / peak, 2),
         "roofline": {"kernel": "paged_decode_append (decode + merge)" if fused else "paged_decode (decode + merge)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
-                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
-        "e2e": {"value": round(aggregate_gbs(step_bytes, e2e_ms / K, ws_n), 1), "unit": "GB/s",
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "copy_same_size_gbs": round(copy_gbs, 1),
+                     "copy_same_size_ms": round(copy_ms, 5),
+                     "frac_of_copy_same_size": round(achieved / copy_gbs, 4),
+                     "copy_same_size_what": f"device copy of {half} B into {half} B (the call's bytes, half read "
+                                            f"and half written, rounded down to 4 KiB), rotating over {R} buffer "
+                                            "pairs, one graph of K copies"},
+        "e2e": {"value": round(step_bytes / (e2e_ms / K * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": ("the call gets HOST buffers: each step's inputs (q, new K/V, tables, lengths) are "
                            "read in place from pinned host memory and its output is written to pinned host "
@@ -515,14 +593,17 @@ def run_gpu(args):
                            "one CUDA graph") if zero_copy else
                           ("per step one H2D of the pinned staged inputs and one D2H of the output, on two copy "
                            "streams ordered by events; double-buffered; the K steps are one CUDA graph"),
-                "staged_copies": {"value": round(aggregate_gbs(step_bytes, staged_ms / K, ws_n), 1),
+                "staged_copies": {"value": round(step_bytes / (staged_ms / K * 1e-3) / 1e9, 1),
                                   "ms_per_step": round(staged_ms / K, 5),
                                   "what": "the same steps with explicit H2D/D2H copies on two copy streams, "
                                           "ordered by events (double-buffered), in one CUDA graph"}},
+        "workloads": others or None,
+        "mixed_step": mixed,
         "prefill_chunk": {"workload": "mixed-step chunk: 512 causal rows at 3584..4095, 28/4 heads, bf16",
                           "bound": "tensor", "achieved": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1),
-                          "peak": _bf16_peak(), "unit": "TFLOP/s",
-                          "frac": round(pf_flops / (pf_ms * 1e-3) / 1e12 / _bf16_peak(), 4),
+                          "peak": bf16_peak, "peak_kind": f"{bf16_kind} bf16 burst (MEASURED_PEAKS.json)",
+                          "unit": "TFLOP/s",
+                          "frac": round(pf_flops / (pf_ms * 1e-3) / 1e12 / bf16_peak, 4),
                           "avg_launch_ms": round(pf_ms, 5), "flops_per_launch": pf_flops},
         "swap_blocks": {"workload": "4096 scattered blocks of the 7B layout (K and V), device <-> pinned host",
                         "bytes_per_call": sw_bytes, "device_to_host_gbs": round(sw_out, 1),
@@ -531,19 +612,126 @@ def run_gpu(args):
                                                 "host_to_device": round(sw_link[1], 1)}},
         "cache_ops": cache_ops,
         "host_plan_us": round(host_plan_us, 1),
-        "host_step": host_step_measure(case) if case.writes else None,
-        "gpu_launches": (3 if case.writes and not fused else 2) * K,   # (kv_write,) decode, merge per step
+        "host_step": host_step,
+        "gpu_launches": launches_per_step * K,
         "unfused_step": None if unfused_ms is None else {
-            "ms_per_step": round(unfused_ms, 5), "value": round(aggregate_gbs(step_bytes, unfused_ms, 1), 1),
+            "ms_per_step": round(unfused_ms, 5), "value": round(step_bytes / (unfused_ms * 1e-3) / 1e9, 1),
             "what": "the same step as pkv_kv_write + pkv_paged_decode (3 launches), one graph of K steps"},
         "clocks": clk.summary(),
     }
-    if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(case, plan, decode_bytes, write_bytes)
-        print(json.dumps(line))
-    if ws_n > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    line["cpu_baseline"] = cpu_baseline(args.workload, case, plan, args.cpu_budget)
+    print(json.dumps(line))
+
+
+def decode_call_measure(n, dev, l2, stream, peak, K, W):
+    """The decode call (the step's call: fused append when the step writes, else decode +
+    merge) on workload n, rotating pool copies when the pool is smaller than 3x L2."""
+    import torch
+    import paged_kv_cache_160_gb300 as pkv
+    import synth
+    from paged_kv_cache_160_gb300.planner import append_slots, product_plan
+    case = synth.CONFIG_BUILDERS[n]()
+    plan = product_plan(case)
+    decode_bytes, write_bytes, tokens = workload_bytes(case, plan)
+    R = rotation(case, l2)
+    kcs, vcs, descs = device_case(pkv, case, dev, R)
+    del case.k_cache, case.v_cache
+    q = case.q.to(dev)
+    out = torch.empty_like(q)
+    tables = torch.tensor(plan.tables, dtype=torch.int32, device=dev)
+    lens = torch.tensor(plan.lens, dtype=torch.int32, device=dev)
+    max_len = max(plan.lens)
+    part = case.partition_size
+    ws = torch.zeros(pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                                    case.head_dim, case.block_size, max_len, part),
+                     dtype=torch.uint8, device=dev)
+    fused = case.writes and append_slots(case, plan) == list(plan.slots)
+    k_new = case.k_new.to(dev) if fused else None
+    v_new = case.v_new.to(dev) if fused else None
+
+    def call(k):
+        r = k % R
+        if fused:
+            pkv.pkv_paged_decode_append(out, q, k_new, v_new, kcs[r], vcs[r], descs[r], tables, lens, max_len,
+                                        case.scale, part, ws, stream)
+        else:
+            pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, part, ws,
+                                 stream)
+
+    n_calls = max(5, min(K, 40)) if decode_bytes > 1e9 else K
+    ms = graph_ms(stream, call, n_calls, max(3, min(W, 5)))
+    assert pkv.pkv_get_device_error(stream) == 0
+    nbytes = decode_bytes + (write_bytes if fused else 0)
+    res = {"workload": WORKLOADS[n], "call": "pkv_paged_decode_append + merge" if fused else
+           "pkv_paged_decode + merge", "bytes_per_call": nbytes, "attended_tokens": tokens,
+           "ms_per_call": round(ms, 5), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+           "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4),
+           "seq_tokens_per_s": round(tokens / (ms * 1e-3), 1), "calls_timed": n_calls,
+           "l2": f"rotating {R} pool copies" if R > 1 else "one pool copy larger than 3x L2"}
+    del kcs, vcs, descs
+    torch.cuda.empty_cache()
+    return res
+
+
+def mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak):
+    """The mixed chunked-prefill + decode step as one graph per step: kv_write of all 640 new
+    rows (128 decode tokens, 512 chunk rows), paged_prefill_chunk of the 512-row chunk at
+    positions 3584..4095, paged_decode of the 128 sequences (+ merge), then copy_blocks of the
+    64 shared-prefix pairs.  K steps in one graph, rotating pool copies."""
+    import torch
+    import paged_kv_cache_160_gb300 as pkv
+    import synth
+    from paged_kv_cache_160_gb300.planner import product_plan
+    case = synth.mixed_config()
+    plan = product_plan(case)
+    assert not plan.cows, "the mixed step's decode tokens need no copy-on-write"
+    work = mixed_step_work(case, plan)
+    R = rotation(case, l2)
+    kcs, vcs, descs = device_case(pkv, case, dev, R)
+    ch = case.chunk
+    q = case.q.to(dev)
+    out = torch.empty_like(q)
+    k_all = torch.cat([case.k_new, ch.k_new]).to(dev)
+    v_all = torch.cat([case.v_new, ch.v_new]).to(dev)
+    slots = torch.tensor(list(plan.slots) + list(plan.chunk_slots), dtype=torch.int64, device=dev)
+    tables = torch.tensor(plan.tables, dtype=torch.int32, device=dev)
+    lens = torch.tensor(plan.lens, dtype=torch.int32, device=dev)
+    max_len = max(plan.lens)
+    ws = torch.zeros(pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                                    case.head_dim, case.block_size, max_len, 0),
+                     dtype=torch.uint8, device=dev)
+    cq = ch.q.to(dev)
+    cout = torch.empty_like(cq)
+    cu = torch.tensor([0, ch.q_len], dtype=torch.int32, device=dev)
+    st0 = torch.tensor([ch.prefix_len], dtype=torch.int32, device=dev)
+    ctab = torch.tensor([plan.chunk_table], dtype=torch.int32, device=dev)
+    pairs = torch.tensor(plan.share_pairs, dtype=torch.int32, device=dev)
+
+    def step(k):
+        r = k % R
+        pkv.pkv_kv_write(k_all, v_all, slots, kcs[r], vcs[r], descs[r], stream)
+        pkv.pkv_paged_prefill_chunk(cout, cq, cu, st0, ch.q_len, kcs[r], vcs[r], descs[r], ctab, case.scale, stream)
+        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, 0, ws, stream)
+        pkv.pkv_copy_blocks(kcs[r], vcs[r], descs[r], pairs, stream)
+
+    ms = graph_ms(stream, step, K, W)
+    assert pkv.pkv_get_device_error(stream) == 0
+    res = {"workload": "mixed chunked-prefill + decode step: 512-row causal chunk at 3584..4095 over its paged "
+                       "prefix, 128 decode seqs with context_lens U[256,4096] (seed 1605), 28/4 heads, head_dim 128, "
+                       "bf16; kv_write 640 rows, then prefill chunk and paged_decode, then copy_blocks 64 pairs",
+           "ms_per_step": round(ms, 5), "launches_per_step": 5,
+           "what": "one CUDA graph of K steps: pkv_kv_write, pkv_paged_prefill_chunk, pkv_paged_decode "
+                   "(decode + merge), pkv_copy_blocks",
+           "bytes_per_step": work["bytes"], "flops_per_step": work["flops"],
+           "gbs": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
+           "tflops": round(work["flops"] / (ms * 1e-3) / 1e12, 1),
+           "seq_tokens_per_s": round(work["tokens"] / (ms * 1e-3), 1),
+           "parts": {k: work[k] for k in ("decode_bytes", "write_bytes", "prefill_bytes", "copy_bytes",
+                                          "prefill_flops", "decode_flops")},
+           "l2": f"rotating {R} pool copies" if R > 1 else "one pool copy larger than 3x L2"}
+    del kcs, vcs, descs
+    torch.cuda.empty_cache()
+    return res
 
 
 def host_step_measure(case, n_steps: int = 20) -> dict:
@@ -553,9 +741,9 @@ def host_step_measure(case, n_steps: int = 20) -> dict:
     import ctypes
     from paged_kv_cache_160_gb300 import BlockManager
     from paged_kv_cache_160_gb300._binding import lib
-    from tests.harness import _import_all, max_blocks_of
+    from paged_kv_cache_160_gb300.planner import import_all, max_blocks_of
     bm = BlockManager(case.num_blocks, case.block_size)
-    _import_all(bm, case)
+    import_all(bm, case)
     n = case.num_seqs
     mb = max_blocks_of(case) + -(-n_steps // case.block_size) + 1
     seqs = (ctypes.c_int64 * n)(*range(n))
@@ -587,27 +775,8 @@ def cache_ops_measure(pkv, case, plan, kc, vc, desc, k_new, v_new, slots, write_
     src = sorted(used)[:n]
     pr = torch.tensor(list(zip(src, free[:n])), dtype=torch.int32, device=kc.device)
     block_bytes = kc[0].numel() * kc.element_size()
-
-    def timed(fn):
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                fn()
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-            for _ in range(iters):
-                fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-        stream.synchronize()
-        return a.elapsed_time(b) / iters
-
-    kw_ms = timed(lambda: pkv.pkv_kv_write(k_new, v_new, slots, kc, vc, desc))
-    cb_ms = timed(lambda: pkv.pkv_copy_blocks(kc, vc, desc, pr))
+    kw_ms = graph_ms(stream, lambda k: pkv.pkv_kv_write(k_new, v_new, slots, kc, vc, desc, stream), iters, 3)
+    cb_ms = graph_ms(stream, lambda k: pkv.pkv_copy_blocks(kc, vc, desc, pr, stream), iters, 3)
     assert pkv.pkv_get_device_error(stream) == 0
     cb_bytes = 2 * 2 * n * block_bytes                    # K and V blocks, read and written
     return {"kv_write": {"tokens": len(plan.slots), "bytes": write_bytes, "avg_launch_ms": round(kw_ms, 5),
@@ -624,7 +793,7 @@ def prefill_measure(dev, iters: int = 30):
     import torch
     import paged_kv_cache_160_gb300 as pkv
     import synth
-    from tests.harness import append_slots, product_plan
+    from paged_kv_cache_160_gb300.planner import product_plan
     case = synth.mixed_config()
     plan = product_plan(case)
     ch = case.chunk
@@ -640,7 +809,7 @@ def prefill_measure(dev, iters: int = 30):
     s = torch.cuda.Stream(device=dev)
 
     def run():
-        pkv.pkv_paged_prefill_chunk(out, q, cu, st0, ch.q_len, kc, vc, desc, tab, case.scale)
+        pkv.pkv_paged_prefill_chunk(out, q, cu, st0, ch.q_len, kc, vc, desc, tab, case.scale, s)
 
     with torch.cuda.stream(s):
         run()
@@ -660,8 +829,7 @@ def prefill_measure(dev, iters: int = 30):
     s.synchronize()
     assert pkv.pkv_get_device_error(s) == 0
     ms = sum(a.elapsed_time(b) for a, b in zip(ea, eb)) / iters
-    pairs = sum(ch.prefix_len + r + 1 for r in range(ch.q_len))
-    flops = 4 * case.head_dim * pairs * case.num_heads
+    flops, _ = prefill_work(case, plan)
     return ms, flops
 
 
@@ -713,92 +881,127 @@ def swap_measure(dev, n_blocks: int = 4096, iters: int = 10):
     return nbytes / (res[0] * 1e-3) / 1e9, nbytes / (res[1] * 1e-3) / 1e9, nbytes, link
 
 
-def _oracle_step(case, plan, seqs):
-    """The oracle (as it stands) on a subset of the step: its KV write and decode.  The sampled
-    sequences' blocks are gathered into a pool of their own first (tables and slots renumbered),
-    so the oracle's copy-on-return KV write copies only that pool."""
-    import numpy as np
-    from oracle import cache_ops, paged_attention as pa
-    from tests.harness import codes, q_f64
-    bs = case.block_size
-    used = sorted({b for i in seqs for b in plan.tables[i] if b >= 0})
-    new_id = {b: n for n, b in enumerate(used)}
-    k, v = codes(case.k_cache)[used], codes(case.v_cache)[used]
-    tables = [[new_id[b] for b in plan.tables[i] if b >= 0] for i in seqs]
-    if case.writes:
-        slots = [new_id[plan.slots[i] // bs] * bs + plan.slots[i] % bs for i in seqs]
-        k, v = cache_ops.kv_write(k, v, codes(case.k_new)[seqs], codes(case.v_new)[seqs], slots)
-    ks = case.k_scale.numpy().astype(np.float64) if case.k_scale is not None else None
-    vs = case.v_scale.numpy().astype(np.float64) if case.v_scale is not None else None
-    pa.decode_attention(q_f64(case.q)[seqs], k, v, case.kv_dtype, tables, [plan.lens[i] for i in seqs], case.scale,
-                        ks, vs)
-
+# ---------------------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------------------
 
 def _sample_bytes(case, plan, seqs):
     """Algorithmic bytes of the sampled sequences' share of the step (their rows counted per
     sequence, as the oracle reads them)."""
     Hkv, D = case.num_kv_heads, case.head_dim
     kv_elt = 1 if case.kv_dtype == "e4m3" else 2
-    rows = sum(plan.lens[i] for i in seqs)
+    rows = sum(plan["lens"][i] for i in seqs)
     n_w = len(seqs) if case.writes else 0
     return (2 * rows * Hkv * D * kv_elt + 2 * len(seqs) * case.num_heads * D * 2 + 4 * len(seqs)
             + 2 * 2 * n_w * Hkv * D * kv_elt + 8 * n_w), rows
 
 
-def cpu_baseline(case, plan, decode_bytes, write_bytes, budget_s: float = 12.0):
-    """Times the fp64 oracle on the host cores, single-threaded BLAS, cycling over the batch."""
-    seqs_all = list(range(case.num_seqs))
-    done_bytes = done_tokens = 0
-    n_seq = 0
-    per = 8 if max(plan.lens) <= 8192 else 1          # long sequences: one per oracle call
+_W_CASE = None
+_W_PLAN = None
+
+
+def _oracle_worker_init(workload: int) -> None:
+    """Each worker process builds the (seeded, identical) workload and plans it with the
+    oracle's own block manager, so no pool crosses a process boundary."""
+    global _W_CASE, _W_PLAN
+    import synth
+    from oracle.workload import plan_step
+    _W_CASE = synth.CONFIG_BUILDERS[workload]()
+    _W_PLAN = plan_step(_W_CASE)
+
+
+def _oracle_task(seqs):
+    from oracle.workload import decode_sample
+    decode_sample(_W_CASE, _W_PLAN["tables"], _W_PLAN["lens"], _W_PLAN["slots"], list(seqs))
+    return _sample_bytes(_W_CASE, _W_PLAN, seqs)
+
+
+def _groups(case, plan, per: int):
+    return [list(range(i, min(i + per, case.num_seqs))) for i in range(0, case.num_seqs, per)]
+
+
+def cpu_baseline(workload: int, case, plan_unused, budget_s: float) -> dict:
+    """Times the fp64 oracle (kv_write + decode, as it stands) on the host cores: once in this
+    process on one core, once over a spawned pool of one process per core (each with one BLAS
+    thread), each for about budget_s seconds of whole-batch passes."""
+    import multiprocessing as mp
+    from oracle.workload import plan_step
+    global _W_CASE, _W_PLAN
+    _W_CASE, _W_PLAN = case, plan_step(case)
+    per = 8 if max(_W_PLAN["lens"]) <= 8192 else 1
+    groups = _groups(case, _W_PLAN, per)
+    # one core
+    done_b = done_rows = n_seq = 0
     t0 = time.perf_counter()
     i = 0
-    while time.perf_counter() - t0 < budget_s:         # about budget_s of CPU work
-        seqs = [seqs_all[(i + j) % case.num_seqs] for j in range(per)]
-        _oracle_step(case, plan, seqs)
-        b, rows = _sample_bytes(case, plan, seqs)
-        done_bytes += b
-        done_tokens += rows
+    while time.perf_counter() - t0 < budget_s:
+        seqs = groups[i % len(groups)]
+        b, rows = _oracle_task(seqs)
+        done_b += b
+        done_rows += rows
         n_seq += len(seqs)
-        i += per
-    dt = time.perf_counter() - t0
-    return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "seq_tokens_per_s": round(done_tokens / dt, 1),
-            "sample": f"fp64 numpy oracle (kv_write + decode) on {n_seq} sequence-steps of the same workload, "
-                      f"{per} sequences per call, {dt:.1f} s wall, 1 BLAS thread"}
+        i += 1
+    dt1 = time.perf_counter() - t0
+    one = {"value": round(done_b / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "seq_tokens_per_s": round(done_rows / dt1, 1),
+           "sample": f"{n_seq} sequence-steps of the workload, {per} sequences per oracle call, {dt1:.1f} s wall"}
+    # all cores: whole-batch passes until the budget is spent
+    cores = os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(workload,)) as pool:
+        pool.map(_oracle_task, [[0]] * cores, chunksize=1)          # every worker built its case
+        fine = [[s] for s in range(case.num_seqs)] if per > 1 else groups
+        done_b = done_rows = n_seq = passes = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < budget_s or passes == 0:
+            for b, rows in pool.imap_unordered(_oracle_task, fine, chunksize=1):
+                done_b += b
+                done_rows += rows
+            n_seq += case.num_seqs
+            passes += 1
+        dtn = time.perf_counter() - t0
+    alln = {"value": round(done_b / dtn / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "seq_tokens_per_s": round(done_rows / dtn, 1),
+            "sample": f"{passes} whole-batch passes ({n_seq} sequence-steps), one sequence per task over "
+                      f"{cores} spawned processes with one BLAS thread each, {dtn:.1f} s wall"}
+    return {"value": alln["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "seq_tokens_per_s": alln["seq_tokens_per_s"],
+            "sample": "fp64 numpy oracle (kv_write + decode) on the same workload; " + alln["sample"],
+            "single_core": one, "all_cores": alln}
 
 
 def run_reference(args):
-    """The oracle as the reference arm: each step is a bounded sample (4 sequences)."""
+    """The oracle as the reference arm: every step is the whole batch's kv_write + decode, as
+    the oracle stands, over a spawned pool of one process per host core."""
+    import multiprocessing as mp
     import synth
-    from tests.harness import oracle_plan
-    ws_n, rank, _ = _dist()
-    if rank != 0:
-        return
+    from oracle.workload import plan_step
     case = synth.CONFIG_BUILDERS[args.workload]()
-    plan = oracle_plan(case)
-    per = 4 if max(plan.lens) <= 8192 else 1
-    if True:
-        for k in range(args.warmup):
-            _oracle_step(case, plan, [(k * per + j) % case.num_seqs for j in range(per)])
+    plan = plan_step(case)
+    cores = os.cpu_count() or 1
+    per = 1
+    tasks = _groups(case, plan, per)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(args.workload,)) as pool:
+        pool.map(_oracle_task, [[0]] * cores, chunksize=1)
+        for _ in range(args.warmup):
+            list(pool.imap_unordered(_oracle_task, tasks, chunksize=1))
         tot_b = tot_rows = 0
         t0 = time.perf_counter()
-        for k in range(args.steps):
-            seqs = [((args.warmup + k) * per + j) % case.num_seqs for j in range(per)]
-            _oracle_step(case, plan, seqs)
-            b, rows = _sample_bytes(case, plan, seqs)
-            tot_b += b
-            tot_rows += rows
+        for _ in range(args.steps):
+            for b, rows in pool.imap_unordered(_oracle_task, tasks, chunksize=1):
+                tot_b += b
+                tot_rows += rows
         dt = time.perf_counter() - t0
     value = tot_b / dt / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws_n,
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOADS[args.workload], "sample_per_step": f"{per} sequences"},
+            "data": "synthetic", "config": {"workload": WORKLOADS[args.workload], "sample_per_step": "the whole batch"},
             "seq_tokens_per_s": round(tot_rows / dt, 1),
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{per} sequences of the workload per step (kv_write + decode), fp64 numpy, "
-                                       "1 BLAS thread"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"every step is the whole batch's kv_write + decode, one sequence per task "
+                                       f"over {cores} spawned processes with one BLAS thread each (fp64 numpy)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -811,9 +1014,14 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS),
                     help="2: the 7B GQA decode step (default, the headline); 3-5: the other decode workloads")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the other workloads and the mixed step (quicker runs)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work per CPU-baseline leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if refuse_multi_gpu(args):
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -42,3 +42,38 @@ def test_e4m3_rows_are_one_byte_and_no_write():
     plan = product_plan(case)
     decode, write = _closed_form(lens, 2, 32, 8, 128, 1, 0, 0)
     assert bench.workload_bytes(case, plan) == (decode, write, sum(lens))
+
+
+def test_prefill_and_mixed_step_work_closed_forms():
+    # chunk of n rows at positions p0..p0+n-1: sum over rows of (p0 + r + 1) attended keys
+    p0, n = 40, 20
+    case = synth.make_decode_case("acct_mixed", 13, [30, 17], 8, 2, 64, "bf16", "bf16", chunk=(p0, n),
+                                  copy_pairs=2)
+    plan = product_plan(case)
+    flops, nbytes = bench.prefill_work(case, plan)
+    pairs = n * p0 + n * (n + 1) // 2
+    assert flops == 4 * 64 * pairs * 8
+    assert nbytes == 2 * (p0 + n) * 2 * 64 * 2 + 2 * n * 8 * 64 * 2 + 4 * len(plan.chunk_table)
+    w = bench.mixed_step_work(case, plan)
+    decode, _, tokens = bench.workload_bytes(case, plan)
+    T = 2 + n                                       # one decode token per sequence + the chunk rows
+    block = 2 * 16 * 64 * 2
+    assert w["write_bytes"] == 2 * 2 * T * 2 * 64 * 2 + 8 * T
+    assert w["copy_bytes"] == 2 * 2 * 2 * block + 8 * 2
+    assert w["bytes"] == decode + w["write_bytes"] + nbytes + w["copy_bytes"]
+    assert w["flops"] == flops + 4 * 64 * tokens * 8
+
+
+def test_bench_refuses_more_than_one_gpu():
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--steps", "3"],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and "unavailable" in d
