@@ -255,7 +255,10 @@ PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype 
  *   max_q_len     host upper bound of the chunks' lengths (sizes the grid)
  * Supported: f16/bf16 cache with the same q dtype, head_dim 128, block_size 16 or 32,
  * num_heads / num_kv_heads in 1..8.  Tensor cores (tcgen05, TMEM accumulators), K/V
- * tiles fetched by TMA straight from the physical blocks.
+ * tiles fetched by TMA straight from the physical blocks and multicast to the four CTAs
+ * of a cluster that read the same keys.  q, k_cache and v_cache must be device memory of
+ * the current GPU (checked with cudaPointerGetAttributes before anything is enqueued):
+ * host, managed or another GPU's memory returns PKV_ERR_INVALID_ARG.
  */
 PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
                                    const int32_t* cu_q_lens, const int32_t* q_start_pos,

@@ -32,6 +32,11 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// True when p points into memory allocated on the current device (cudaMalloc or a pool
+// allocation), false for host, managed, unregistered or another device's memory, or when the
+// query fails.  The runtime's error state is left clear.
+bool on_current_device(const void* p);
+
 inline int dtype_bytes(pkv_dtype d) { return d == PKV_FP8_E4M3 ? 1 : 2; }
 
 // Shared checks of a cache descriptor; returns PKV_OK or the failing status.

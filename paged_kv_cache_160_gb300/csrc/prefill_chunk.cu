@@ -519,6 +519,11 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   if (!(scale > 0.f)) return PKV_ERR_INVALID_ARG;          // the softmax takes max(s) * scale
   if (int64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size >= (int64_t(1) << 31))
     return PKV_ERR_UNSUPPORTED;
+  // The K/V tiles are multicast across the CTAs of a cluster, so q and both caches must be
+  // device memory of the current GPU: host, managed or another GPU's memory is refused
+  // before any tensor map is built.
+  if (!on_current_device(q) || !on_current_device(k_cache) || !on_current_device(v_cache))
+    return PKV_ERR_INVALID_ARG;
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
 

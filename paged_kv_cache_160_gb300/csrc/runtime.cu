@@ -60,6 +60,17 @@ unsigned* error_word_ptr() {
   return g_dev[d].err;
 }
 
+bool on_current_device(const void* p) {
+  const int d = current_device();
+  if (d < 0 || !p) return false;
+  cudaPointerAttributes a = {};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == d;
+}
+
 int num_sms() {
   int d = current_device();
   if (d < 0 || d >= kMaxDevices) return 0;

@@ -148,3 +148,37 @@ def test_mixed_workload_chunk():
                      prefill_heads=[0, 6, 7, 20, 27])
     err = max_abs_err(dev.prefill, ref.prefill)
     assert err <= TOL["bf16"], err
+
+
+def test_refuses_q_or_caches_that_are_not_memory_of_this_gpu():
+    """The prefill kernel multicasts its K/V tiles across a cluster, so the call takes q and the
+    caches only in device memory of the current GPU: a pinned host k_cache, v_cache or q is
+    refused with PKV_ERR_INVALID_ARG before anything is enqueued (out stays untouched)."""
+    import ctypes
+    import paged_kv_cache_160_gb300 as pkv
+    from paged_kv_cache_160_gb300._binding import pkv_dtype_of
+    c = _case(7, [(20, 30)], 4, 2, "bf16")
+    dev = torch.device("cuda")
+    kc, vc, q = c["k"].to(dev), c["v"].to(dev), c["q"].to(dev)
+    hk, hv, hq = c["k"].pin_memory(), c["v"].pin_memory(), c["q"].pin_memory()
+    desc = pkv.cache_desc(kc)
+    out = torch.full_like(q, float("nan"))
+    cu = torch.tensor(c["cu"], dtype=torch.int32, device=dev)
+    st = torch.tensor(c["starts"], dtype=torch.int32, device=dev)
+    tab = torch.tensor(c["tables"], dtype=torch.int32, device=dev)
+
+    def call(qq, kk, vv):
+        return pkv.lib.pkv_paged_prefill_chunk(out.data_ptr(), qq.data_ptr(), pkv_dtype_of(q), cu.data_ptr(),
+                                               st.data_ptr(), 1, q.shape[0], c["max_q"], q.shape[1], kk.data_ptr(),
+                                               vv.data_ptr(), ctypes.byref(desc), tab.data_ptr(), tab.shape[1],
+                                               1 / math.sqrt(128), torch.cuda.current_stream().cuda_stream)
+
+    assert call(q, hk, vc) == 1
+    assert call(q, kc, hv) == 1
+    assert call(hq, kc, vc) == 1
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()
+    assert call(q, kc, vc) == 0                    # the same call on device memory runs
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    assert pkv.pkv_get_device_error() == 0

@@ -202,11 +202,24 @@ def test_prefill_chunk_equals_causal_sdpa(prefix, n):
 
 
 def test_waste_is_at_most_one_partial_block_per_sequence():
-    lens = list(np.random.default_rng(1).integers(1, 3000, size=200))
+    """"PagedAttention: manage the KV cache like virtual memory" §3.1: only a sequence's last
+    block can be partly empty.  Grow 200 sequences of random lengths token by token on the
+    oracle's block manager and count, for each, the reserved slots it does not use."""
+    from oracle.block_manager import BlockManagerModel
+    rng = np.random.default_rng(1)
     bs = 16
-    for L in lens:
-        waste = -(-L // bs) * bs - L
-        assert 0 <= waste <= bs - 1
+    lens = [int(x) for x in rng.integers(1, 600, size=200)]
+    bm = BlockManagerModel(sum(-(-L // bs) for L in lens), bs)
+    for i, L in enumerate(lens):
+        bm.allocate(i, 1)
+        for _ in range(L - 1):
+            bm.append_slot(i)
+    tables, got = bm.export(list(range(len(lens))), max(-(-L // bs) for L in lens))
+    assert got == lens
+    assert bm.num_free() == 0                                   # every block is in some table
+    for t, L in zip(tables, lens):
+        reserved = bs * sum(1 for b in t if b >= 0)
+        assert 0 <= reserved - L <= bs - 1
 
 
 # ---------------------------------------------------------------------------------------
