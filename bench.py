@@ -278,7 +278,7 @@ def run_gpu(args):
 
     import paged_kv_cache_160_gb300 as pkv
     import synth
-    from paged_kv_cache_160_gb300.planner import append_slots, product_plan
+    from paged_kv_cache_160_gb300.planner import append_slots, decode_tile_rows, product_plan
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -401,6 +401,15 @@ def run_gpu(args):
     copy_ms = graph_ms(stream, lambda k: dst[k % R].copy_(src[k % R]), K, W)
     copy_gbs = 2 * half / (copy_ms * 1e-3) / 1e9
     del src, dst
+    # The decode's own memory ceiling: the same K/V tiles read by the same kind of pipeline
+    # (pkv_stream_tiles: persistent grid, 12 warps x 2 bulk-copy stages per SM), no compute.
+    tile_rows = decode_tile_rows(case, plan)
+    rows_t = torch.tensor(tile_rows, dtype=torch.int32, device=dev)
+    csum = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream_ms = graph_ms(stream, lambda k: pkv.pkv_stream_tiles(kcs[k % R], vcs[k % R], descs[k % R], rows_t, csum,
+                                                                stream), K, W)
+    tile_read_bytes = 2 * len(tile_rows) * 16 * case.head_dim * (1 if case.kv_dtype == "e4m3" else 2)
+    assert pkv.pkv_get_device_error(stream) == 0
 
     # ---- end to end, staged: explicit copies on copy streams --------------------------------
     host_parts = [case.q, torch.tensor(plan.tables, dtype=torch.int32), torch.tensor(plan.lens, dtype=torch.int32)]
@@ -584,7 +593,13 @@ def run_gpu(args):
                      "frac_of_copy_same_size": round(achieved / copy_gbs, 4),
                      "copy_same_size_what": f"device copy of {half} B into {half} B (the call's bytes, half read "
                                             f"and half written, rounded down to 4 KiB), rotating over {R} buffer "
-                                            "pairs, one graph of K copies"},
+                                            "pairs, one graph of K copies",
+                     "tile_stream_ms": round(stream_ms, 5),
+                     "tile_stream_gbs": round(tile_read_bytes / (stream_ms * 1e-3) / 1e9, 1),
+                     "frac_of_tile_stream": round(stream_ms / dec_avg_ms, 4),
+                     "tile_stream_what": f"pkv_stream_tiles over the call's {len(tile_rows)} K/V tiles "
+                                         f"({tile_read_bytes} B): the decode's memory pipeline with no compute, "
+                                         "same rotation, one graph of K calls"},
         "e2e": {"value": round(step_bytes / (e2e_ms / K * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "copies": ("the call gets HOST buffers: each step's inputs (q, new K/V, tables, lengths) are "

@@ -275,6 +275,19 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtype q
 PKV_API pkv_status pkv_get_device_error(int* code, pkv_stream_t stream);
 
 /*
+ * Measurement aid, not part of the method: reads the num_tiles K/V tiles whose first pool
+ * rows are tile_rows[i] (16 rows of one (block, kv head), in K and in V) with the memory
+ * pipeline pkv_paged_decode uses (persistent grid, 12 warps per SM, two stages of one K and
+ * one V tile per warp, bulk asynchronous copies) and computes nothing but a checksum, XORed
+ * into *checksum.  Timed on the tiles of a decode call, it is the memory ceiling of that
+ * call.  Rows outside the pool are skipped and flagged PKV_DEVERR_BLOCK_ID.
+ *   tile_rows (device) int32 [num_tiles]; checksum (device) one uint32
+ */
+PKV_API pkv_status pkv_stream_tiles(const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                    const int32_t* tile_rows, int num_tiles, unsigned* checksum,
+                                    pkv_stream_t stream);
+
+/*
  * Diagnostic of the failure path every kernel shares: one warp waits on an mbarrier that
  * nothing arrives on, with the same bounded wait the kernels use, for limit_ns (0 < limit_ns
  * <= 1 s), then sets PKV_DEVERR_TIMEOUT and returns.  Nothing faults or hangs; the context

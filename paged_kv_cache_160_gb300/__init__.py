@@ -22,5 +22,6 @@ from ._binding import (  # noqa: F401
     pkv_paged_decode_noalloc,
     pkv_noalloc_scratch_bytes,
     pkv_paged_prefill_chunk,
+    pkv_stream_tiles,
     pkv_swap_blocks,
 )

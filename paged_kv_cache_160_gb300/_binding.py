@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_copy_blocks.argtypes = [c_void_p, c_void_p, POINTER(CacheDesc), c_void_p, c_int, c_void_p]
     lib.pkv_check_bounded_wait.restype = S
     lib.pkv_check_bounded_wait.argtypes = [ctypes.c_uint64, c_void_p]
+    lib.pkv_stream_tiles.restype = S
+    lib.pkv_stream_tiles.argtypes = [c_void_p, c_void_p, POINTER(CacheDesc), c_void_p, c_int, c_void_p, c_void_p]
     lib.pkv_swap_blocks.restype = S
     lib.pkv_swap_blocks.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, POINTER(CacheDesc),
                                     c_void_p, c_int, c_void_p]
@@ -201,6 +203,16 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, desc: CacheDes
 def pkv_check_bounded_wait(limit_ns: int, stream=None) -> None:
     """Run the shared bounded wait on a barrier nothing arrives on; it sets the timeout bit."""
     _check(lib.pkv_check_bounded_wait(int(limit_ns), _stream(stream)), "pkv_check_bounded_wait")
+
+
+def pkv_stream_tiles(k_cache: torch.Tensor, v_cache: torch.Tensor, desc: CacheDesc, tile_rows: torch.Tensor,
+                     checksum: torch.Tensor, stream=None) -> None:
+    """Read the listed K/V tiles with the decode's memory pipeline and nothing else (a
+    measurement of the decode's memory ceiling); tile_rows holds each tile's first pool row."""
+    assert tile_rows.dtype == torch.int32 and checksum.dtype == torch.int32 and checksum.numel() >= 1
+    _check(lib.pkv_stream_tiles(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                _dev(tile_rows, "tile_rows"), tile_rows.numel(), _dev(checksum, "checksum"),
+                                _stream(stream)), "pkv_stream_tiles")
 
 
 def _dev_or_pinned(t: torch.Tensor, name: str) -> int:

@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["runtime.cu", "cache_ops.cu", "paged_decode.cu", "paged_decode_noalloc.cu", "prefill_chunk.cu",
-           "block_manager.cpp"]
+           "stream_tiles.cu", "block_manager.cpp"]
 
 
 def nvcc() -> str:

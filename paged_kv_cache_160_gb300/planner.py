@@ -82,3 +82,17 @@ def append_slots(case, plan: Plan) -> List[int]:
     slots the fused append call writes."""
     bs = case.block_size
     return [plan.tables[i][(L - 1) // bs] * bs + (L - 1) % bs if L >= 1 else -1 for i, L in enumerate(plan.lens)]
+
+
+def decode_tile_rows(case, plan: Plan) -> List[int]:
+    """First pool row of every 16-row tile a decode call reads, in its order: sequence, kv
+    head, tile.  A block of B tokens holds B / 16 tiles at rows (block * Hkv + h) * B + 16 * i."""
+    bs, hkv = case.block_size, case.num_kv_heads
+    rows = []
+    for t, L in zip(plan.tables, plan.lens):
+        ntiles = -(-L // 16)
+        for h in range(hkv):
+            for i in range(ntiles):
+                blk = t[(16 * i) // bs]
+                rows.append((blk * hkv + h) * bs + (16 * i) % bs)
+    return rows

@@ -70,6 +70,11 @@ def test_argument_checks_run_on_host_without_gpu():
     assert L.pkv_swap_blocks(16, 16, 0, 16, 16, 8, ctypes.byref(desc), 16, 2, None) == 1
     assert L.pkv_swap_blocks(16, 16, 8, 16, 16, 8, ctypes.byref(desc), None, 2, None) == 1
     assert L.pkv_swap_blocks(16, 16, 8, 16, 16, 8, ctypes.byref(desc), 16, 0, None) == 0
+    # the tile-stream measurement: misaligned pool, missing rows or checksum; no tiles is fine
+    assert L.pkv_stream_tiles(24, 16, ctypes.byref(desc), 16, 4, 16, None) == 1
+    assert L.pkv_stream_tiles(16, 16, ctypes.byref(desc), None, 4, 16, None) == 1
+    assert L.pkv_stream_tiles(16, 16, ctypes.byref(desc), 16, 4, None, None) == 1
+    assert L.pkv_stream_tiles(16, 16, ctypes.byref(desc), 16, 0, 16, None) == 0
     # the bounded-wait diagnostic takes a limit in (0, 1 s]
     assert L.pkv_check_bounded_wait(0, None) == 1
     assert L.pkv_check_bounded_wait(2_000_000_000, None) == 1

@@ -77,3 +77,19 @@ def test_bench_refuses_more_than_one_gpu():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["n_gpus"] == 2 and "unavailable" in d
+
+
+def test_decode_tile_rows_follow_the_block_tables():
+    """Every tile row is the pool row of logical token 16 * i of its sequence (address
+    translation of Lecture 33 §2.2), for 16- and 32-token blocks."""
+    from paged_kv_cache_160_gb300.planner import decode_tile_rows
+    for bs in (16, 32):
+        case = synth.make_decode_case("acct_rows", 21, [5, 40, 33], 4, 2, 64, "f16", "f16", block_size=bs)
+        plan = product_plan(case)
+        rows = decode_tile_rows(case, plan)
+        want = []
+        for t, L in zip(plan.tables, plan.lens):
+            for h in range(2):
+                for j in range(0, L, 16):
+                    want.append((t[j // bs] * 2 + h) * bs + j % bs)
+        assert rows == want
