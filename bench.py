@@ -801,10 +801,11 @@ def cache_ops_measure(pkv, case, plan, kc, vc, desc, k_new, v_new, slots, write_
             "timing": f"one CUDA graph of {iters} back-to-back calls between events, per-call average"}
 
 
-def prefill_measure(dev, iters: int = 30):
+def prefill_measure(dev, iters: int = 30, reps: int = 10):
     """paged_prefill_chunk on the mixed workload's chunk: 512 causal rows at positions
-    3584..4095 over the sequence's paged cache, 28/4 heads, bf16.  CUDA-graph replays timed
-    with events; FLOPs = 4 * head_dim * (attended query-key pairs) * heads."""
+    3584..4095 over the sequence's paged cache, 28/4 heads, bf16.  One CUDA graph of `reps`
+    back-to-back calls, replayed `iters` times between events: the time per call without the
+    graph's launch; FLOPs = 4 * head_dim * (attended query-key pairs) * heads."""
     import torch
     import paged_kv_cache_160_gb300 as pkv
     import synth
@@ -831,7 +832,8 @@ def prefill_measure(dev, iters: int = 30):
     s.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
-        run()
+        for _ in range(reps):
+            run()
     ea = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
     eb = [torch.cuda.Event(enable_timing=True) for _ in range(iters)]
     with torch.cuda.stream(s):
@@ -843,7 +845,7 @@ def prefill_measure(dev, iters: int = 30):
             eb[k].record(s)
     s.synchronize()
     assert pkv.pkv_get_device_error(s) == 0
-    ms = sum(a.elapsed_time(b) for a, b in zip(ea, eb)) / iters
+    ms = sum(a.elapsed_time(b) for a, b in zip(ea, eb)) / (iters * reps)
     flops, _ = prefill_work(case, plan)
     return ms, flops
 

@@ -84,6 +84,43 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b) {
   return pack2<kBF16>(a, b);
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane, from raw words.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Three-input maximum (one instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two fp32 values in one 64-bit register pair, for the packed fp32 instructions.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+// a * b + c and a + b on both halves, rounded to nearest (the same results as fmaf / +).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -143,12 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_v_full[i], 1);
       mbar_init(&bar_v_empty[i], kCluster);
     }
+    // The softmax warps signal P and the row-value swaps once per warp (lane 0, after the
+    // warp's own accesses): 8 arrivals a phase.
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_p_full[i], 256);
+      mbar_init(&bar_p_full[i], 8);
     }
-    mbar_init(&bar_xchg[0], 256);
-    mbar_init(&bar_xchg[1], 256);
+    mbar_init(&bar_xchg[0], 8);
+    mbar_init(&bar_xchg[1], 8);
     // PV_t's completion arrives on bar_pv_done[t % kSBufs].  A waiter for PV_t is always at most
     // one phase behind that barrier (PV_{t+kSBufs} needs P_{t+kSBufs}, which the softmax has not
     // produced yet), so waiting by phase parity is exact.  One barrier for every PV would not
@@ -359,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto swap_halves = [&](float mine, float& theirs) -> bool {
       const int b = n_swaps & 1;
       row_xchg[b][half][r] = mine;
-      mbar_arrive(&bar_xchg[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_xchg[b]);
       const bool done = mbar_wait(&bar_xchg[b], uint32_t(n_swaps >> 1) & 1u);
       theirs = row_xchg[b][half ^ 1][r];
       ++n_swaps;
@@ -445,9 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32u(tS(j) + lane_off + 32 * half, w);
       tmem_wait_st();
       l += lsum;
-      fence_proxy_async_smem();                              // the zeroed V rows, if any
+      if (kb + kTile > ctx) fence_proxy_async_smem();        // the zeroed V rows, to the tensor cores
       tc_fence_before();
-      mbar_arrive(&bar_p_full[j % kSBufs]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p_full[j % kSBufs]);
     }
     if (ok) ok = mbar_wait(&bar_pv_done[(nt - 1) % kSBufs], uint32_t((nt - 1) / kSBufs) & 1u);
     // Row sum = the two halves' partial sums (both used the same m).
@@ -484,6 +525,551 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   cluster_sync();                                            // no peer sends to this CTA any more
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+
+// ---------------------------------------------------------------------------------------
+// Two query heads per CTA, the key range split in two, in clusters of four CTAs.
+//
+// The query heads of a GQA group read the same K/V.  A CTA here takes two heads of one kv head
+// (128 rows each), so every K/V tile it receives feeds 256 query rows.  A cluster is two
+// adjacent q-tiles x two halves of their key range: the two CTAs of a half read the same keys,
+// each issues half of every tile's TMA boxes and multicasts them to both; the two halves of a
+// q-tile merge their partial results at the end.
+//   warp 0     : TMA producer: Q of both heads once, then its half of the boxes of K and V
+//                of the half's key tiles (2 stages each), multicast to the q-tile partner.  A
+//                stage is refilled once both CTAs' tensor-core commits have released it.
+//   warp 1     : TMEM owner (512 columns: S_A | S_B | O_A | O_B) and MMA issuer, in the
+//                fixed order S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ... so that
+//                one head's softmax overlaps the other head's products.
+//   warps 2-5  : softmax of head A, warps 6-9: head B; one query row per thread.  The row's
+//                128 scores are read from TMEM once; the max uses 3-input max, P = 2^(s*c - m)
+//                uses packed fp32x2 multiply-add and add; P goes over S in TMEM; O is rescaled
+//                only when the row max grows by more than 2^8.
+// At the end the first-half CTA of a q-tile finishes head A and the second-half CTA head B.
+// Each CTA stages the other head's unnormalised O rows and (max, sum) in its idle stages and
+// sends them to its peer with one bulk shared-memory copy; the receiver combines the two parts
+// by log-sum-exp, stages the 16-bit rows in the idle Q area and writes them out coalesced.
+// ---------------------------------------------------------------------------------------
+constexpr int kPairThreads = 320;
+constexpr int kPairKStages = 2;
+constexpr int kPairVStages = 2;
+// The merge's exchange block: [128 rows][kXStride] fp32 O, then 128 row maxima and 128 row sums.
+constexpr int kXStride = kD + 4;
+constexpr int kXBytes = (kTile * kXStride + 2 * kTile) * 4;
+constexpr int kXAreaBytes = (kXBytes + 1023) / 1024 * 1024;
+// Output rows staged as 16-bit values in the Q area, padded by 16 bytes per row.
+constexpr int kOStride = kD * 2 + 16;
+static_assert(kTile * kOStride <= 2 * kTileBytes, "the staged output rows fit in the Q area");
+// Q_A, Q_B, 2 K and 2 V stages (192 KB); after the main loop the K/V stages and 8 KB past
+// them hold the receive and staging areas of the merge (200 KB in all).
+constexpr int kPairKVBytes = (kPairKStages + kPairVStages) * kTileBytes;
+constexpr int kPairSmemBytes = 2 * kTileBytes + (2 * kXAreaBytes > kPairKVBytes ? 2 * kXAreaBytes : kPairKVBytes);
+
+__device__ __forceinline__ uint32_t peer_smem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// Copies `bytes` (a multiple of 16) from this CTA's shared memory to a peer CTA's, completing
+// on the peer's mbarrier; dst and bar are shared::cluster addresses (from mapa).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Non-blocking check of a phase whose arrivals include other CTAs' (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// One arrival on an mbarrier of a peer CTA (a shared::cluster address from mapa), as a bare
+// signal: relaxed, it orders none of this thread's memory accesses.  Every use below signals
+// an event whose memory effects are ordered otherwise (a tensor-core commit that has been
+// observed, a CTA barrier after the last store to the area, a completed bulk copy).
+__device__ __forceinline__ void remote_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_k_full[kPairKStages], bar_k_empty[kPairKStages],
+      bar_v_full[kPairVStages], bar_v_empty[kPairVStages], bar_s_full[2], bar_p_full[2], bar_pv_done[2], bar_x,
+      bar_ready, bar_done;
+  __shared__ uint32_t tmem_base_sh;
+
+  const int qt = blockIdx.x, slot = blockIdx.y, c = blockIdx.z >> 1;
+  const uint32_t crank = cluster_ctarank();                 // (q-tile of the pair) + 2 * (key half)
+  const uint32_t khalf = crank >> 1;
+  const uint16_t mc_mask = uint16_t(3u << (2 * khalf));     // the two CTAs reading this half's keys
+  const int q0 = p.cu_q_lens[c];
+  const int qlen = p.cu_q_lens[c + 1] - q0;
+  const int r0 = qt * kTile;
+  const int r0_pair = (qt & ~1) * kTile;
+  // Every decision before the first cluster barrier is the same for all CTAs of the cluster.
+  if (qlen <= 0 || r0_pair >= qlen) return;
+  const int start = p.q_start_pos[c];
+  const int ctx = start + qlen;                              // keys 0 .. ctx-1 exist
+  if (start < 0 || ctx > p.max_blocks * p.block_size) {
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
+    return;
+  }
+  // Both q-tiles of the pair walk the keys the later one needs (the earlier one finds the
+  // extra keys in its rows' future, masked); a q-tile past the chunk still takes part.
+  const int kmax = start + min(qlen, r0_pair + 2 * kTile);
+  const int nt = (kmax + kTile - 1) / kTile;
+  const int mid = (nt + 1) / 2;
+  const int j0 = khalf ? mid : 0;                            // this CTA's key tiles j0 .. j0 + n - 1
+  const int n = khalf ? nt - mid : mid;
+  const int G = p.num_heads / p.num_kv_heads;
+  const int spg = (G + 1) / 2;                               // head pairs (slots) per kv head
+  const int h = slot / spg;
+  const int hq0 = h * G + 2 * (slot % spg);
+  const int hq1 = 2 * (slot % spg) + 1 < G ? hq0 + 1 : hq0;  // an odd group's last slot repeats a head
+  const int nb = (ctx + kBS - 1) / kBS;
+  const int32_t* table = p.block_tables + int64_t(c) * p.max_blocks;
+
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem) & 1023u) {                              // the 128-byte swizzle needs 1 KB alignment
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
+    return;
+  }
+  uint8_t* sQ = smem;                                        // [head][64-dim half][128 rows]
+  uint8_t* sK = smem + 2 * kTileBytes;
+  uint8_t* sV = smem + (2 + kPairKStages) * kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmq);
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+    mbar_init(&bar_q, 1);
+    // A stage is free again once both CTAs reading this half's keys have released it: each
+    // CTA's tensor-core commit arrives on the stage's empty barrier in both.
+    for (int i = 0; i < kPairKStages; ++i) {
+      mbar_init(&bar_k_full[i], 1);
+      mbar_init(&bar_k_empty[i], 2);
+    }
+    for (int i = 0; i < kPairVStages; ++i) {
+      mbar_init(&bar_v_full[i], 1);
+      mbar_init(&bar_v_empty[i], 2);
+    }
+    // One phase per key tile each.  A head's softmax waits on its pv_done only for the
+    // product of the previous tile, and the next product needs this tile's P first, so the
+    // barrier is never two phases ahead of its waiter.
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_s_full[x], 1);
+      mbar_init(&bar_p_full[x], 4);                          // one arrival per softmax warp
+      mbar_init(&bar_pv_done[x], 1);
+    }
+    // The merge's one bulk copy from the peer completes this barrier's first phase.
+    mbar_init(&bar_x, 1);
+    mbar_arrive_expect_tx(&bar_x, kXAreaBytes);
+    mbar_init(&bar_ready, 1);                                // the peer's receive area is free
+    mbar_init(&bar_done, 1);                                 // the peer has this CTA's whole block
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                            // every CTA's barriers are initialised
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    const uint64_t pol_q = l2_policy_evict_first();
+    const uint64_t pol_kv = l2_policy_evict_last();          // re-read by the other query heads
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, 2 * kTileBytes);
+      tma_load_3d(sQ, &tmq, &bar_q, 0, hq0, q0 + r0, pol_q);
+      tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq0, q0 + r0, pol_q);
+      tma_load_3d(sQ + kTileBytes, &tmq, &bar_q, 0, hq1, q0 + r0, pol_q);
+      tma_load_3d(sQ + kTileBytes + kHalfBytes, &tmq, &bar_q, 64, hq1, q0 + r0, pol_q);
+    }
+    // Pool rows of the sequence's 16-row units, 32 per window (4 tiles); units past the
+    // sequence map to block 0 (their rows are masked / zeroed).
+    auto load_window = [&](int w) -> int {
+      const int lb = 32 * w + lane;
+      int pb = 0;
+      if (lb < nb) {
+        pb = table[lb >> p.tile_shift];
+        if (pb < 0 || pb >= p.num_blocks) {
+          set_error(p.err, PKV_DEVERR_BLOCK_ID);
+          pb = 0;
+        }
+      }
+      return (pb * p.num_kv_heads + h) * p.block_size + (lb & ((1 << p.tile_shift) - 1)) * kBS;
+    };
+    struct Window {
+      int cur, nxt, w;
+    };
+    auto seek = [&](Window& win, int j) {
+      while (j / 4 > win.w) {
+        win.cur = win.nxt;
+        ++win.w;
+        win.nxt = load_window(win.w + 1);
+      }
+    };
+    Window wk{load_window(j0 / 4), load_window(j0 / 4 + 1), j0 / 4};
+    Window wv = wk;
+    auto issue_k = [&](uint8_t* dst, uint64_t* bar, int j) {
+      seek(wk, j);
+      const int first = (8 * j) % 32;
+      if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
+      __syncwarp();
+      const int blk = lane - first;
+      if (blk >= 0 && blk < kTile / kBS) {                   // this CTA's half: the 64-dim half hf
+        const int hf = int(crank & 1u);
+        tma_load_3d_mc(dst + hf * kHalfBytes + blk * (kBlockBytes / 2), &tmk, bar, 0, wk.cur, hf, mc_mask, pol_kv);
+      }
+    };
+    auto issue_v = [&](uint8_t* dst, uint64_t* bar, int j) {
+      seek(wv, j);
+      const int first = (8 * j) % 32;
+      if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
+      __syncwarp();
+      const int blk = lane - first;
+      if (blk >= 0 && blk < kTile / kBS && uint32_t(blk & 1) == (crank & 1u))   // every other block
+        tma_load_3d_mc(dst + blk * kBlockBytes, &tmv, bar, 0, wv.cur, 0, mc_mask, pol_kv);
+    };
+    // The empty barriers also collect the partner CTA's releases: acquire at cluster scope.
+    auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
+      uint32_t r = 0;
+      if (lane == 0) r = mbar_test_cluster(bar, parity) ? 1u : 0u;
+      return __shfl_sync(0xffffffffu, r, 0) != 0;
+    };
+    int kt = 0, vt = 0;                                      // tiles issued, counted from j0
+    uint64_t t0 = 0;
+    bool ok = true;
+    while (ok && (kt < n || vt < n)) {
+      bool progress = false;
+      if (kt < n && (kt < kPairKStages ||
+                     ready(&bar_k_empty[kt % kPairKStages], uint32_t((kt - kPairKStages) / kPairKStages) & 1u))) {
+        issue_k(sK + (kt % kPairKStages) * kTileBytes, &bar_k_full[kt % kPairKStages], j0 + kt);
+        ++kt;
+        progress = true;
+      }
+      if (vt < kt && (vt < kPairVStages ||
+                      ready(&bar_v_empty[vt % kPairVStages], uint32_t((vt - kPairVStages) / kPairVStages) & 1u))) {
+        issue_v(sV + (vt % kPairVStages) * kTileBytes, &bar_v_full[vt % kPairVStages], j0 + vt);
+        ++vt;
+        progress = true;
+      }
+      if (!progress) __nanosleep(100);
+      uint32_t give_up = 0;
+      if (lane == 0) {
+        if (progress) {
+          t0 = 0;
+        } else if (t0 == 0) {
+          t0 = global_timer_ns();
+        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+          set_error(p.err, PKV_DEVERR_TIMEOUT);
+          give_up = 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
+    }
+    // Drain: the last loads of each stage have landed, and the partner's releases of the last
+    // tiles have reached this CTA's barriers, before the CTA may leave.
+    if (lane == 0) {
+      for (int t = kt - kPairKStages < 0 ? 0 : kt - kPairKStages; t < kt; ++t)
+        (void)mbar_wait(&bar_k_full[t % kPairKStages], uint32_t(t / kPairKStages) & 1u);
+      for (int t = vt - kPairVStages < 0 ? 0 : vt - kPairVStages; t < vt; ++t)
+        (void)mbar_wait(&bar_v_full[t % kPairVStages], uint32_t(t / kPairVStages) & 1u);
+      for (int t = kt - kPairKStages < 0 ? 0 : kt - kPairKStages; t < kt; ++t)
+        (void)mbar_wait(&bar_k_empty[t % kPairKStages], uint32_t(t / kPairKStages) & 1u);
+      for (int t = vt - kPairVStages < 0 ? 0 : vt - kPairVStages; t < vt; ++t)
+        (void)mbar_wait(&bar_v_empty[t % kPairVStages], uint32_t(t / kPairVStages) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc_s = umma_idesc_f16(kBF16, 128, 128, false, false);
+    const uint32_t idesc_o = umma_idesc_f16(kBF16, 128, 128, false, true);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+    bool ok = mbar_wait(&bar_q, 0);
+    // S_x(t) = Q_x K_t^T into TMEM columns 128x .. 128x + 127.
+    auto issue_s = [&](int x, int t) -> bool {
+      const int st = t % kPairKStages;
+      if (!mbar_wait(&bar_k_full[st], uint32_t(t / kPairKStages) & 1u)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        umma_f16(tmem + 128 * x, umma_sdesc_sw128(aQ + x * kTileBytes + off, 16, 1024),
+                 umma_sdesc_sw128(aK + st * kTileBytes + off, 16, 1024), idesc_s, kk > 0);
+      }
+      umma_commit(&bar_s_full[x]);
+      if (x == 1) umma_commit_mc(&bar_k_empty[st], mc_mask); // both heads have read K_t: release it in both CTAs
+      return true;
+    };
+    // O_x += P_x(t) V_t, P_x in the first 64 columns of S_x.
+    auto issue_pv = [&](int x, int t) -> bool {
+      const int st = t % kPairVStages;
+      if (!mbar_wait(&bar_p_full[x], uint32_t(t) & 1u)) return false;
+      if (!mbar_wait(&bar_v_full[st], uint32_t(t / kPairVStages) & 1u)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        umma_f16_ts(tmem + 256 + 128 * x, tmem + 128 * x + 8 * kk,
+                    umma_sdesc_sw128(aV + st * kTileBytes + kk * kBlockBytes, kBlockBytes / 2, 1024), idesc_o,
+                    t > 0 || kk > 0);
+      }
+      umma_commit(&bar_pv_done[x]);
+      if (x == 1) umma_commit_mc(&bar_v_empty[st], mc_mask); // both heads have read V_t: release it in both CTAs
+      return true;
+    };
+    if (ok && n > 0) ok = issue_s(0, 0) && issue_s(1, 0);
+    for (int t = 0; ok && t < n; ++t) {
+      ok = issue_pv(0, t) && (t + 1 >= n || issue_s(0, t + 1)) && issue_pv(1, t) && (t + 1 >= n || issue_s(1, t + 1));
+    }
+    if (!ok) set_error(p.err, PKV_DEVERR_TIMEOUT);
+  }
+
+  // ---------------- softmax: warps 2-5 head A, 6-9 head B; one row per thread ----------------
+  const int x = (warp - 2) >> 2;                             // head of this warpgroup (softmax warps)
+  const int r = 32 * (warp & 3) + lane;                      // TMEM lane == row of the tile
+  const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+  const int qrow = r0 + r;
+  float m = -INFINITY, l = 0.f;                              // m in scaled log2 units
+  if (warp >= 2) {
+    const int pos = start + qrow;                            // absolute position of this query
+    const float sl = p.scale_log2;                           // > 0, so max(s) * sl = max(s * sl)
+    const uint32_t tS = tmem + 128 * x + lane_off, tO = tmem + 256 + 128 * x + lane_off;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int j = j0 + t;
+      if (!(ok = mbar_wait(&bar_s_full[x], uint32_t(t) & 1u))) break;
+      __syncwarp();
+      tc_fence_after();
+      const int lim = min(pos + 1, ctx) - j * kTile;         // keys 0 .. lim-1 of the tile are valid
+      // The whole row of S in registers: one read of TMEM per tile.
+      float s[kTile];
+#pragma unroll
+      for (int cc = 0; cc < kTile / 32; ++cc) tmem_ld32(tS + 32 * cc, *reinterpret_cast<float(*)[32]>(s + 32 * cc));
+      tmem_wait_ld();
+      if (lim < kTile) {                                     // the tile crosses this row's diagonal or the end
+#pragma unroll
+        for (int i = 0; i < kTile; ++i) s[i] = i < lim ? s[i] : -INFINITY;
+      }
+      float mraw;
+      {
+        float c4[4] = {s[0], s[1], s[2], s[3]};              // four independent chains of 3-input max
+#pragma unroll
+        for (int i = 4; i < kTile; i += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) c4[u] = fmax3(c4[u], s[i + 2 * u], s[i + 2 * u + 1]);
+        }
+        mraw = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+      }
+      const float mt = mraw * sl;
+      const bool grow = mt > m + kRescaleThreshold;          // also true for the first tile
+      const float m_prev = m;
+      if (grow) m = mt;
+      // The sequence's last key tile may reach past its end: zero those V rows so that
+      // 0 * garbage cannot turn into NaN inside the PV product (both heads write the same zeros).
+      const int kb = j * kTile;
+      if (kb + kTile > ctx) {
+        if (!(ok = mbar_wait(&bar_v_full[t % kPairVStages], uint32_t(t / kPairVStages) & 1u))) break;
+        if (kb + r >= ctx) {
+          const uint32_t vrow = smem_u32(sV + (t % kPairVStages) * kTileBytes) + (r / kBS) * kBlockBytes + (r % kBS) * 128;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) sts128(vrow + hf * (kBlockBytes / 2) + cc * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      // P = 2^(s * sl - m) as 16-bit pairs written over this tile's S (keys 2e, 2e+1 go to
+      // column e), two elements per packed fp32 operation.  A row with no valid key so far has
+      // m = -inf and every s = -inf: m = 0 then gives P = 0.
+      const float mu = m == -INFINITY ? 0.f : m;
+      const uint64_t sl2 = pack_f32x2(sl, sl), nm2 = pack_f32x2(-mu, -mu);
+      uint64_t acc0 = pack_f32x2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+      for (int hb = 0; hb < 4; ++hb) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * hb + 2 * e;
+          const uint64_t x2 = fma_f32x2(pack_f32x2(s[c0], s[c0 + 1]), sl2, nm2);
+          const float pa = fast_exp2(lo_f32(x2)), pb = fast_exp2(hi_f32(x2));
+          const uint64_t p2 = pack_f32x2(pa, pb);
+          if (e & 1) acc1 = add_f32x2(acc1, p2);
+          else acc0 = add_f32x2(acc0, p2);
+          w[e] = pack_out<kBF16>(pa, pb);
+        }
+        tmem_st16u(tS + 16 * hb, w);
+      }
+      const uint64_t acc = add_f32x2(acc0, acc1);
+      const float lsum = lo_f32(acc) + hi_f32(acc);
+      if (__any_sync(0xffffffffu, grow && t >= 1)) {
+        // A row whose max grew rescales O, once the previous PV product has landed in it (the
+        // S values are dead by now, so the rescale does not add to the loop's live registers).
+        if (!(ok = mbar_wait(&bar_pv_done[x], uint32_t(t - 1) & 1u))) break;
+        __syncwarp();
+        tc_fence_after();
+        const float alpha = (grow && m_prev != -INFINITY) ? fast_exp2(m_prev - m) : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float v[32];
+          tmem_ld32(tO + 32 * cc, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tmem_st32(tO + 32 * cc, v);
+        }
+        if (grow) l *= alpha;
+      }
+      tmem_wait_st();
+      l += lsum;
+      if (kb + kTile > ctx) fence_proxy_async_smem();        // the zeroed V rows, to the tensor cores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p_full[x]);
+    }
+    if (ok && n > 0) ok = mbar_wait(&bar_pv_done[x], uint32_t(n - 1) & 1u);
+    if (!ok && r == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
+    __syncwarp();
+    tc_fence_after();
+  }
+
+  // ---------------- merge the two parts of the key range ----------------
+  // The sending warpgroup stages its head's unnormalised O rows and (max, sum) in its own idle
+  // K/V stages; once the peer says its receive area is free, one bulk copy moves the block
+  // there, completing on the peer's bar_x.  Layout of both areas: [row][kXStride] fp32 O (rows
+  // padded by 16 bytes so that the threads' 16-byte row accesses spread over all banks), then
+  // the rows' max and sum.  Only the two CTAs of a q-tile take part: the peer signals with
+  // remote mbarrier arrivals, and each CTA waits for every arrival aimed at it before it leaves.
+  float* xO = reinterpret_cast<float*>(sK);                  // receive area
+  float* xM = xO + kTile * kXStride;
+  float* xL = xM + kTile;
+  float* yO = reinterpret_cast<float*>(sK + kXAreaBytes);    // staging area
+  float* yM = yO + kTile * kXStride;
+  float* yL = yM + kTile;
+  const uint32_t xpeer = cluster_ctarank() ^ 2u;             // the same q-tile's other key half
+  const int fin = int(cluster_ctarank() >> 1);               // the head this CTA finishes: its key half
+  tc_fence_before();
+  __syncthreads();                                           // this CTA's loads and products are all done
+  tc_fence_after();
+  if (warp >= 2 && x != fin) {
+    const uint32_t tO = tmem + 256 + 128 * x + lane_off;
+    const bool have = n > 0 && m != -INFINITY;
+    const uint32_t row = smem_u32(yO + r * kXStride);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float v[32];
+      tmem_ld32(tO + 32 * cc, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        if (have)
+          sts128(row + (32 * cc + i) * 4, __float_as_uint(v[i]), __float_as_uint(v[i + 1]), __float_as_uint(v[i + 2]),
+                 __float_as_uint(v[i + 3]));
+        else
+          sts128(row + (32 * cc + i) * 4, 0u, 0u, 0u, 0u);
+      }
+    }
+    yM[r] = have ? m : -INFINITY;
+    yL[r] = have ? l : 0.f;
+    fence_proxy_async_smem();                                // the staged rows, to the bulk copy
+    named_barrier_sync(1, 128);                              // the whole warpgroup has staged its rows
+    if (r == 0) {
+      if (mbar_wait(&bar_ready, 0))
+        bulk_copy_to_peer(peer_smem_addr(smem_u32(xO), xpeer), smem_u32(yO), kXAreaBytes,
+                          peer_smem_addr(smem_u32(&bar_x), xpeer));
+      else
+        set_error(p.err, PKV_DEVERR_TIMEOUT);
+      // The staging area is read until the peer has the whole block.
+      if (!mbar_wait(&bar_done, 0)) set_error(p.err, PKV_DEVERR_TIMEOUT);
+    }
+  } else if (warp >= 2) {
+    // Finish this head: take the peer's part, combine the two by log-sum-exp, stage the output
+    // rows in the idle Q area and write them out a row pair per warp instruction.
+    if (r == 0) remote_arrive(peer_smem_addr(smem_u32(&bar_ready), xpeer));   // the receive area is free
+    const bool got = mbar_wait(&bar_x, 0);
+    if (r == 0 && got) remote_arrive(peer_smem_addr(smem_u32(&bar_done), xpeer));
+    __syncwarp();
+    if (!got) {
+      if (r == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
+    } else if (x == 0 || hq1 != hq0) {                       // the whole warp: tcgen05.ld is collective
+      const float mp = xM[r], lp = xL[r];
+      const bool have = n > 0 && m != -INFINITY;
+      const float mo = have ? m : -INFINITY;
+      const float M = fmaxf(mo, mp);
+      const float wo = mo == -INFINITY ? 0.f : fast_exp2(mo - M);
+      const float wp = mp == -INFINITY ? 0.f : fast_exp2(mp - M);
+      const float den = wo * (have ? l : 0.f) + wp * lp;
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      const uint32_t tO = tmem + 256 + 128 * x + lane_off;
+      const float4* po = reinterpret_cast<const float4*>(xO + r * kXStride);
+      const uint32_t orow = smem_u32(sQ) + r * kOStride;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(tO + 32 * cc, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 q = po[8 * cc + i4];
+          const int i = 4 * i4;
+          v[i] = ((have ? wo * v[i] : 0.f) + wp * q.x) * inv;
+          v[i + 1] = ((have ? wo * v[i + 1] : 0.f) + wp * q.y) * inv;
+          v[i + 2] = ((have ? wo * v[i + 2] : 0.f) + wp * q.z) * inv;
+          v[i + 3] = ((have ? wo * v[i + 3] : 0.f) + wp * q.w) * inv;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          sts128(orow + (cc * 4 + q4) * 16, pack_out<kBF16>(v[8 * q4], v[8 * q4 + 1]),
+                 pack_out<kBF16>(v[8 * q4 + 2], v[8 * q4 + 3]), pack_out<kBF16>(v[8 * q4 + 4], v[8 * q4 + 5]),
+                 pack_out<kBF16>(v[8 * q4 + 6], v[8 * q4 + 7]));
+      }
+      __syncwarp();                                          // this warp's 32 rows are staged
+      const int hq = x == 0 ? hq0 : hq1;
+      const int rw = 32 * (warp & 3);
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int rr = rw + 2 * k + (lane >> 4);
+        const uint4 val = lds128(smem_u32(sQ) + rr * kOStride + (lane & 15) * 16);
+        if (r0 + rr < qlen)
+          reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                   ((int64_t(q0) + r0 + rr) * p.num_heads + hq) * (kD * 2))[lane & 15] = val;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -552,6 +1138,28 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.err = err;
 
+  const int G = num_heads / cache->num_kv_heads;
+  if (G >= 2) {
+    // Two query heads of a kv head per CTA; clusters of 2 q-tiles x 2 halves of the key range.
+    const int spg = (G + 1) / 2;
+    if (int64_t(num_chunks) * 2 > 65535 || int64_t(cache->num_kv_heads) * spg > 65535) return PKV_ERR_UNSUPPORTED;
+    auto pk = q_dtype == PKV_BF16 ? prefill_pair_kernel<true> : prefill_pair_kernel<false>;
+    if (cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(((max_q_len + kTile - 1) / kTile + 1) & ~1, cache->num_kv_heads * spg, num_chunks * 2);
+    pc.blockDim = dim3(kPairThreads);
+    pc.dynamicSmemBytes = kPairSmemBytes;
+    pc.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeClusterDimension;
+    pa[0].val.clusterDim.x = 2;
+    pa[0].val.clusterDim.y = 1;
+    pa[0].val.clusterDim.z = 2;
+    pc.attrs = pa;
+    pc.numAttrs = 1;
+    return cudaLaunchKernelEx(&pc, pk, tq, tk, tv, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   auto kern = q_dtype == PKV_BF16 ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return PKV_ERR_CUDA;
