@@ -1034,15 +1034,33 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the other workloads and the mixed step (quicker runs)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work per CPU-baseline leg")
+    ap.add_argument("--part", choices=["prefill"],
+                    help="time one call alone and print its line (a small command to profile): "
+                         "prefill = paged_prefill_chunk on the mixed-step chunk")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if refuse_multi_gpu(args):
         return
-    if args.impl == "reference":
+    if args.part == "prefill":
+        run_part_prefill(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
+
+
+def run_part_prefill(args):
+    """Only the prefill chunk of the mixed step, `args.steps` graph replays of 10 calls."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    ms, flops = prefill_measure(dev, iters=max(1, args.steps))
+    peak, _ = _bf16_peak()
+    tf = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({"part": "prefill_chunk", "workload": "mixed-step chunk: 512 causal rows at 3584..4095, 28/4 heads, bf16",
+                      "avg_launch_ms": round(ms, 5), "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak, 4),
+                      "flops_per_launch": flops}))
 
 
 if __name__ == "__main__":
