@@ -141,9 +141,9 @@ PKV_API pkv_status pkv_swap_blocks(void* dst_k, void* dst_v, int dst_num_blocks,
 /*
  * Workspace bytes pkv_paged_decode needs on the current device: two partial-result
  * slots per worker warp (running max, sum of exponentials and unnormalised output per
- * query head) plus one piece descriptor per (sequence, kv head).  It depends on the
- * device's SM count, not on the context lengths.  The workspace needs no initialisation;
- * each call rewrites what it reads.  Calls that share a workspace must not overlap.
+ * query head).  It depends on the device's SM count and the group size, not on the number
+ * of sequences or the context lengths.  The workspace needs no initialisation; each call
+ * rewrites what it reads.  Calls that share a workspace must not overlap.
  */
 PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                   int block_size, int max_context_len, int partition_size);
@@ -223,9 +223,10 @@ PKV_API pkv_status pkv_paged_decode_append(void* out, const void* q, pkv_dtype q
  * workspace: the library keeps one fixed scratch array of pkv_noalloc_scratch_bytes()
  * (24 MiB) on every device that loads it, resident until the process exits.  Arguments are
  * checked exactly as pkv_paged_decode checks them, in the same order, so an invalid call
- * returns the same status from both entry points.  A valid call that needs more scratch
- * than the array holds (per pkv_decode_workspace_bytes) returns PKV_ERR_WORKSPACE and
- * enqueues nothing.  No call allocates, frees or clears device memory: each call
+ * returns the same status from both entry points.  The scratch a call needs (per
+ * pkv_decode_workspace_bytes) depends on the SM count, the group size and head_dim only;
+ * 24 MiB holds every supported call on a device of up to 252 SMs.  A valid call that needs
+ * more than the array holds returns PKV_ERR_WORKSPACE and enqueues nothing.  No call allocates, frees or clears device memory: each call
  * rewrites the parts of the array it later reads, so leftovers of earlier calls do no
  * harm.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any

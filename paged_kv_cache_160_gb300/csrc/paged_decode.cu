@@ -83,7 +83,6 @@ struct DecodeParams {
   int part_blocks;        // tiles per partition; 0 = balanced split
   int num_workers;        // gridDim.x * worker warps per CTA
   float scale_log2;       // softmax scale * log2(e)
-  int4* seg_desc;         // [num_seqs * num_kv_heads]: (first worker, pieces, first worker's slot parity, 0)
   float2* ml;             // [slots][group] (running max in log2 units, sum of exponentials)
   float* po;              // [slots][group][D] unnormalised partial outputs
   unsigned* err;
@@ -232,7 +231,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       if (cum_nb[s + 1] != cum_nb[s]) continue;
       const int n = Hkv * G * D;
       for (int e = threadIdx.x; e < n; e += blockDim.x) store_out<QT>(p.out, int64_t(s) * n + e, 0.f);
-      if (threadIdx.x < Hkv) p.seg_desc[s * Hkv + threadIdx.x] = make_int4(0, 0, 0, 0);
     }
   };
 
@@ -319,21 +317,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const Tile c = locate_in(t, first.s, last.s);
     return p.block_tables[int64_t(c.s) * p.max_blocks + (c.b >> p.tile_shift)];
   };
-  int bid_cur = load_window(0);                // in flight while the piece count below is worked out
+  int bid_cur = load_window(0);
   int bid_nxt = n > 32 ? load_window(1) : -1;
-
-  // The only piece of this range that can open a segment without closing it is the
-  // range's last one; the merge needs that segment's piece count.  Worker of unit u: the
-  // largest wi with start_of(wi) <= u, i.e. floor(((u + 1) W - 1) / nunits).  Lengths only,
-  // so it is worked out before the wait.
-  int last_np = 1;
-  if (lane == 0) {
-    const Tile& c = last;
-    const int64_t u_end = PB ? int64_t(Hkv) * cum_np[c.s] + int64_t(c.h) * (cum_np[c.s + 1] - cum_np[c.s]) +
-                                   (c.nb - 1) / PB
-                             : int64_t(Hkv) * cum_nb[c.s] + int64_t(c.h) * c.nb + c.nb - 1;
-    last_np = int(((u_end + 1) * W - 1) / nunits) - w + 1;
-  }
 
   // First pool row of tile c in block pb: the (block, kv head) rows start at
   // (pb * Hkv + h) * block_size and a 32-token block holds the tile's 16 rows at offset 0
@@ -622,18 +607,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const float vs = KV == KV_E4M3 ? p.v_scale[tl.h] : 1.f;
     const int h0 = 2 * tq, h1 = 2 * tq + 1;
     const int Hq = Hkv * G;
-    const int seg = tl.s * Hkv + tl.h;
     const int64_t seg_t0 = int64_t(Hkv) * cum_nb[tl.s] + int64_t(tl.h) * tl.nb;
     const int64_t piece_t0 = seg_t0 + piece_b0;
+    // A segment's pieces belong to consecutive workers, one each; the merge kernel works out
+    // which from the lengths.  A piece that starts its worker's range goes to the worker's
+    // first slot (2w), any other to its second (2w + 1): a range holds at most one piece
+    // that starts inside it and runs past its end.
     const bool complete = piece_b0 == 0 && tl.b + 1 == tl.nb;
-    if (piece_b0 == 0 && lane == 0) {
-      // This worker holds the segment's first tile: describe the segment's pieces for the
-      // merge kernel.  Workers w .. w + npieces - 1 cover it, one piece each; worker w's
-      // piece is its first (slot 2w) if the segment starts its range, else its second
-      // (slot 2w + 1).  A segment that starts here and runs past the range is the range's
-      // last, whose piece count the prologue worked out.
-      p.seg_desc[seg] = make_int4(w, complete ? 1 : last_np, piece_t0 == t_begin ? 0 : 1, 0);
-    }
     if (complete) {
       const float inv0 = ls0 > 0.f ? vs / ls0 : 0.f, inv1 = ls1 > 0.f ? vs / ls1 : 0.f;
       const int64_t base = (int64_t(tl.s) * Hq + int64_t(tl.h) * G) * D;
@@ -669,11 +649,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
 struct MergeParams {
   void* out;
-  const int4* seg_desc;
   const float2* ml;
   const float* po;
+  const int32_t* context_lens;
+  int num_seqs;
+  int num_kv_heads;
   int num_segments;       // num_seqs * num_kv_heads
   int group;
+  int max_len;            // the decode call's length clamp
+  int part_blocks;        // the decode call's tiles per partition (0: balanced split)
+  int num_workers;        // the decode call's worker warps
 };
 
 constexpr int kMergeWarps = 8;
@@ -684,21 +669,54 @@ constexpr int kMergeWarps = 8;
 // kChunk pieces' rows; the weights come from warp reductions over the lanes, so the
 // loads of a block of 32 pieces overlap and no exponential sits between a load and the sum.
 template <int QT, int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) split_kv_merge_kernel(const MergeParams p) {
-  griddep_wait();                            // the decode kernel's partials are complete
-  griddep_launch_dependents();               // the next kernel may start its own prologue
+__global__ void __launch_bounds__(kMergeWarps * 32, 2) split_kv_merge_kernel(const MergeParams p) {
   constexpr int kLanesPerHead = D / 4;       // 16-byte chunks of one head's row
   constexpr int kHP = 32 / kLanesPerHead;    // rows per load instruction of the warp
   constexpr int kChunk = 16;                 // loads in flight per lane
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int64_t item = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
-  if (item >= int64_t(p.num_segments) * G) return;
-  const int seg = int(item / G), hh = int(item % G);
-  const int4 d = p.seg_desc[seg];
-  const int w0 = d.x, np = d.y;
-  if (np <= 1) return;
-  auto slot_of = [&](int k) -> int64_t { return k == 0 ? 2 * int64_t(w0) + d.z : 2 * int64_t(w0 + k); };
+  const bool active = item < int64_t(p.num_segments) * G;
+  const int seg = active ? int(item / G) : 0, hh = active ? int(item % G) : 0;
+
+  // The segment's pieces, from the lengths alone and before the wait (so while the decode
+  // grid's last CTAs still run).  The decode kernel splits the flattened units (tiles, or
+  // partitions of part_blocks tiles) of all (sequence, kv head) segments into num_workers
+  // ranges, range w starting at unit floor(w * units / W); the worker of unit u is
+  // floor(((u + 1) W - 1) / units).  The segment's pieces belong to workers w0 .. w0 + np - 1;
+  // worker w0's piece is in its first slot (2 w0) if the segment starts its range, else in its
+  // second (2 w0 + 1), and every later worker's piece is in its first.
+  int w0 = 0, np = 0, z = 0;
+  if (active) {
+    const int S = p.num_seqs, Hkv = p.num_kv_heads, PB = p.part_blocks;
+    const int s = seg / Hkv, h = seg - s * Hkv;
+    int tot = 0, pre = 0, mine = 0;          // units of all sequences, of those before s, of s
+    for (int i = lane; i < S; i += 32) {
+      const int nb = (clamp_len(__ldg(p.context_lens + i), p.max_len) + kBS - 1) / kBS;
+      const int nu = PB ? (nb + PB - 1) / PB : nb;
+      tot += nu;
+      if (i < s) pre += nu;
+      if (i == s) mine = nu;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      pre += __shfl_xor_sync(0xffffffffu, pre, o);
+      mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    }
+    const int64_t units = int64_t(Hkv) * tot;
+    const int64_t W = min(int64_t(p.num_workers), units);
+    if (mine > 0 && W > 0) {
+      const int64_t u0 = int64_t(Hkv) * pre + int64_t(h) * mine, u1 = u0 + mine - 1;
+      w0 = int(((u0 + 1) * W - 1) / units);
+      np = int(((u1 + 1) * W - 1) / units) - w0 + 1;
+      z = int64_t(w0) * units / W == u0 ? 0 : 1;
+    }
+  }
+  griddep_wait();                            // the decode kernel's partials are complete
+  griddep_launch_dependents();               // the next kernel may start its own prologue
+  if (np <= 1) return;                       // empty, or finished by the decode kernel itself
+  auto slot_of = [&](int k) -> int64_t { return k == 0 ? 2 * int64_t(w0) + z : 2 * int64_t(w0 + k); };
   const int rsub = lane / kLanesPerHead, dof = (lane % kLanesPerHead) * 4;
   float M = -INFINITY, den = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int kb = 0; kb < np; kb += 32) {
@@ -766,17 +784,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) split_kv_merge_kernel(const 
 // host side
 // ---------------------------------------------------------------------------------------
 struct Layout {
-  size_t desc = 0, ml = 0, po = 0, total = 0;
+  size_t ml = 0, po = 0, total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int64_t num_slots(int workers) { return 2 * int64_t(workers); }
 
-Layout layout(int num_seqs, int num_kv_heads, int group, int head_dim, int64_t slots) {
+Layout layout(int group, int head_dim, int64_t slots) {
   Layout l;
-  l.desc = 0;
-  l.ml = align256(sizeof(int4) * size_t(num_seqs) * num_kv_heads);
+  l.ml = 0;
   l.po = l.ml + align256(sizeof(float2) * size_t(slots) * group);
   l.total = l.po + align256(sizeof(float) * size_t(slots) * group * head_dim);
   return l;
@@ -811,11 +828,16 @@ pkv_status launch_cfg(DecodeParams prm, const CUtensorMap& tk, const CUtensorMap
   if (launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, tk, tv, prm) != cudaSuccess) return PKV_ERR_CUDA;
   MergeParams mp;
   mp.out = prm.out;
-  mp.seg_desc = prm.seg_desc;
   mp.ml = prm.ml;
   mp.po = prm.po;
+  mp.context_lens = prm.context_lens;
+  mp.num_seqs = prm.num_seqs;
+  mp.num_kv_heads = prm.num_kv_heads;
   mp.num_segments = prm.num_seqs * prm.num_kv_heads;
   mp.group = prm.group;
+  mp.max_len = prm.max_len;
+  mp.part_blocks = prm.part_blocks;
+  mp.num_workers = prm.num_workers;
   const int64_t items = int64_t(mp.num_segments) * mp.group;
   const int mgrid = int((items + kMergeWarps - 1) / kMergeWarps);
   if (launch_pdl(split_kv_merge_kernel<QT, D>, dim3(mgrid), dim3(kMergeWarps * 32), 0, stream, mp) != cudaSuccess)
@@ -859,7 +881,7 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
   const int group = num_heads / num_kv_heads;
   const int workers = decode_grid() * kMaxWarps;
   const int64_t slots = num_slots(workers);
-  return layout(num_seqs, num_kv_heads, group, head_dim, slots).total;
+  return layout(group, head_dim, slots).total;
 }
 
 }  // extern "C"
@@ -901,7 +923,7 @@ pkv_status decode_check(const void* out, const void* q, pkv_dtype q_dtype, int n
     return PKV_ERR_UNSUPPORTED;
   const int grid = decode_grid();
   if (int64_t(grid) * kMaxWarps >= (int64_t(1) << 16)) return PKV_ERR_UNSUPPORTED;
-  *need = layout(num_seqs, cache->num_kv_heads, group, D, num_slots(grid * kMaxWarps)).total;
+  *need = layout(group, D, num_slots(grid * kMaxWarps)).total;
   return PKV_OK;
 }
 
@@ -925,7 +947,7 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs
   const int64_t max_len = std::min<int64_t>(int64_t(max_blocks_per_seq) * cache->block_size, max_context_len);
   const int grid = decode_grid();
   const int part_blocks = partition_size / kBS;
-  const Layout lay = layout(num_seqs, cache->num_kv_heads, group, D, num_slots(grid * kMaxWarps));
+  const Layout lay = layout(group, D, num_slots(grid * kMaxWarps));
   unsigned* err = error_word_ptr();
   if (!err) return PKV_ERR_CUDA;
 
@@ -965,7 +987,6 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs
   prm.tile_shift = cache->block_size == 32 ? 1 : 0;
   prm.part_blocks = part_blocks;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  prm.seg_desc = reinterpret_cast<int4*>(ws + lay.desc);
   prm.ml = reinterpret_cast<float2*>(ws + lay.ml);
   prm.po = reinterpret_cast<float*>(ws + lay.po);
   prm.err = err;
