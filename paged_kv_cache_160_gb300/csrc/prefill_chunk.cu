@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 //                only when the row max grows by more than 2^8.
 // At the end the first-half CTA of a q-tile finishes head A and the second-half CTA head B.
 // Each CTA stages the other head's unnormalised O rows and (max, sum) in its idle stages and
-// sends them to its peer with one bulk shared-memory copy; the receiver combines the two parts
+// sends them to its peer with bulk shared-memory copies; the receiver combines the two parts
 // by log-sum-exp, stages the 16-bit rows in the idle Q area and writes them out coalesced.
 // ---------------------------------------------------------------------------------------
 constexpr int kPairThreads = 320;
@@ -563,6 +563,8 @@ constexpr int kPairVStages = 2;
 constexpr int kXStride = kD + 4;
 constexpr int kXBytes = (kTile * kXStride + 2 * kTile) * 4;
 constexpr int kXAreaBytes = (kXBytes + 1023) / 1024 * 1024;
+static_assert((32 * kXStride * 4) % 16 == 0 && (kTile * kXStride * 4) % 16 == 0,
+              "each warp's rows, and the max and sum arrays after them, start and end on 16 bytes");
 // Output rows staged as 16-bit values in the Q area, padded by 16 bytes per row.
 constexpr int kOStride = kD * 2 + 16;
 static_assert(kTile * kOStride <= 2 * kTileBytes, "the staged output rows fit in the Q area");
@@ -583,10 +585,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "r"(src), "r"(bytes), "r"(bar)
                : "memory");
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Non-blocking check of a phase whose arrivals include other CTAs' (acquire at cluster scope).
@@ -690,9 +688,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(&bar_p_full[x], 4);                          // one arrival per softmax warp
       mbar_init(&bar_pv_done[x], 1);
     }
-    // The merge's one bulk copy from the peer completes this barrier's first phase.
+    // The merge's bulk copies from the peer complete this barrier's first phase.
     mbar_init(&bar_x, 1);
-    mbar_arrive_expect_tx(&bar_x, kXAreaBytes);
+    mbar_arrive_expect_tx(&bar_x, kXBytes);
     mbar_init(&bar_ready, 1);                                // the peer's receive area is free
     mbar_init(&bar_done, 1);                                 // the peer has this CTA's whole block
     fence_mbar_init();
@@ -967,8 +965,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   // ---------------- merge the two parts of the key range ----------------
   // The sending warpgroup stages its head's unnormalised O rows and (max, sum) in its own idle
-  // K/V stages; once the peer says its receive area is free, one bulk copy moves the block
-  // there, completing on the peer's bar_x.  Layout of both areas: [row][kXStride] fp32 O (rows
+  // K/V stages; once the peer says its receive area is free, bulk copies (one set per warp)
+  // move the block there, completing on the peer's bar_x.  Layout of both areas: [row][kXStride] fp32 O (rows
   // padded by 16 bytes so that the threads' 16-byte row accesses spread over all banks), then
   // the rows' max and sum.  Only the two CTAs of a q-tile take part: the peer signals with
   // remote mbarrier arrivals, and each CTA waits for every arrival aimed at it before it leaves.
@@ -1004,16 +1002,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     yM[r] = have ? m : -INFINITY;
     yL[r] = have ? l : 0.f;
     fence_proxy_async_smem();                                // the staged rows, to the bulk copy
-    named_barrier_sync(1, 128);                              // the whole warpgroup has staged its rows
-    if (r == 0) {
-      if (mbar_wait(&bar_ready, 0))
-        bulk_copy_to_peer(peer_smem_addr(smem_u32(xO), xpeer), smem_u32(yO), kXAreaBytes,
-                          peer_smem_addr(smem_u32(&bar_x), xpeer));
-      else
+    __syncwarp();                                            // this warp's 32 rows are staged
+    if (lane == 0) {
+      // Each warp sends its own rows as soon as they are staged: four copies in flight.
+      const int w32 = 32 * (warp & 3);
+      if (mbar_wait(&bar_ready, 0)) {
+        const uint32_t bar = peer_smem_addr(smem_u32(&bar_x), xpeer);
+        bulk_copy_to_peer(peer_smem_addr(smem_u32(xO + w32 * kXStride), xpeer), smem_u32(yO + w32 * kXStride),
+                          32 * kXStride * 4, bar);
+        bulk_copy_to_peer(peer_smem_addr(smem_u32(xM + w32), xpeer), smem_u32(yM + w32), 32 * 4, bar);
+        bulk_copy_to_peer(peer_smem_addr(smem_u32(xL + w32), xpeer), smem_u32(yL + w32), 32 * 4, bar);
+      } else {
         set_error(p.err, PKV_DEVERR_TIMEOUT);
-      // The staging area is read until the peer has the whole block.
-      if (!mbar_wait(&bar_done, 0)) set_error(p.err, PKV_DEVERR_TIMEOUT);
+      }
     }
+    // The staging area is read until the peer has the whole block.
+    if (r == 0 && !mbar_wait(&bar_done, 0)) set_error(p.err, PKV_DEVERR_TIMEOUT);
   } else if (warp >= 2) {
     // Finish this head: take the peer's part, combine the two by log-sum-exp, stage the output
     // rows in the idle Q area and write them out a row pair per warp instruction.
