@@ -628,6 +628,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t crank = cluster_ctarank();                 // (q-tile of the pair) + 2 * (key half)
   const uint32_t khalf = crank >> 1;
   const uint16_t mc_mask = uint16_t(3u << (2 * khalf));     // the two CTAs reading this half's keys
+  // Launched as a programmatic dependent: the CTA may start while the previous kernel runs,
+  // and reads nothing that kernel may write before this point.
+  griddep_wait();
   const int q0 = p.cu_q_lens[c];
   const int qlen = p.cu_q_lens[c + 1] - q0;
   const int r0 = qt * kTile;
@@ -981,6 +984,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   tc_fence_before();
   __syncthreads();                                           // this CTA's loads and products are all done
   tc_fence_after();
+  griddep_launch_dependents();                               // the next kernel may start its prologue
   if (warp >= 2 && x != fin) {
     const uint32_t tO = tmem + 256 + 128 * x + lane_off;
     const bool have = n > 0 && m != -INFINITY;
@@ -1155,13 +1159,15 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
     pc.blockDim = dim3(kPairThreads);
     pc.dynamicSmemBytes = kPairSmemBytes;
     pc.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute pa[1];
+    cudaLaunchAttribute pa[2];
     pa[0].id = cudaLaunchAttributeClusterDimension;
     pa[0].val.clusterDim.x = 2;
     pa[0].val.clusterDim.y = 1;
     pa[0].val.clusterDim.z = 2;
+    pa[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pa[1].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
-    pc.numAttrs = 1;
+    pc.numAttrs = 2;
     return cudaLaunchKernelEx(&pc, pk, tq, tk, tv, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   }
   auto kern = q_dtype == PKV_BF16 ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
