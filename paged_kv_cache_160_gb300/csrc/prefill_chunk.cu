@@ -6,30 +6,13 @@
 // p = q_start + r and attends keys 0..p of its sequence, read through the block table
 // (§2.2–§2.3) — the same paged cache the decode kernel reads.
 //
-// GB300 design (one CTA per 128 query rows of one query head, 1 CTA per SM):
-//   warp 0             : TMA producer — Q once (128 rows x 128 dims), then per 128-key tile
-//                        the 8 physical 16-row blocks of K and of V, gathered by block id
-//                        (the block table is read 32 entries at a time, lane-parallel, one
-//                        window ahead).  K lands as [64-dim half][block][16 rows] (two 2-D
-//                        boxes per block), so its 8-row groups are evenly spaced and one
-//                        N = 128 MMA covers the tile; V lands as [block][half][16 rows] (one
-//                        3-D box per block).  K and V (3 stages each) run ahead, each stage
-//                        refilled once every CTA of the cluster has released it.
-//   warp 1             : owns 512 TMEM columns; one thread issues tcgen05.mma —
-//                        S_j = Q K_j^T (M = N = 128, K = 128, both operands K-major in smem,
-//                        column n of S = key n of the tile) into one of three TMEM S buffers, and
-//                        O += P_j V_j into the TMEM O accumulator, with P read from TMEM (it
-//                        overwrites S_j in place) and V from shared memory as an MN-major
-//                        operand.  S of later tiles overlaps the softmax of earlier ones, and
-//                        the softmax never waits for a PV product unless it must rescale O.
-//   warps 2..9         : softmax, two warpgroups; each thread owns one query row (TMEM lane)
-//                        and one half of its 128 columns, the halves swap only the tile's row
-//                        max.  Causal mask on diagonal tiles, online softmax in base 2
-//                        (2^(s*scale*log2e - m): one FFMA and one ex2 per score), P (bf16/f16)
-//                        stored to TMEM over the tile's S.  The running max used for the
-//                        exponents is only moved (and O rescaled in TMEM) when the row max
-//                        grows by more than 2^8, so most tiles skip the rescale; the final
-//                        division by the same-base sum keeps the result exact.
+// GB300 design: one CTA per SM holds two row blocks of 128 query rows that read the same K/V
+// (two query heads of a kv head, or two adjacent query tiles of a head when each query head has
+// its own kv head), and walks half of their key range; the CTA with the other half finishes the
+// rows with it.  Roles, TMEM layout and the merge are described above the kernel below.
+// K and V are gathered from the paged cache by TMA, one box per 16-row half block (K, in two
+// 64-dim halves so that one N = 128 product covers a tile) or per block (V), by physical block
+// id from the block table, read 32 entries at a time, lane-parallel, one window ahead.
 // Every wait is bounded; a timeout sets PKV_DEVERR_TIMEOUT and the CTA drains and exits.
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -40,8 +23,7 @@ namespace {
 constexpr int kBS = 16;        // rows per TMA box: a 16-token block, or half of a 32-token one
 constexpr int kD = 128;
 constexpr int kTile = 128;                    // query rows per CTA and keys per iteration
-constexpr int kThreads = 320;                 // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
-constexpr uint32_t kTmemCols = 512;           // S0 | S1 | S2 | O, 128 columns each
+constexpr uint32_t kTmemCols = 512;           // S_A | S_B | O_A | O_B, 128 columns each
 constexpr int kHalfBytes = kTile * 128;       // [128 rows][64 elements] of 2 bytes = 16 KB
 constexpr int kTileBytes = 2 * kHalfBytes;    // one 128 x 128 operand = 32 KB
 // A V tile holds 8 blocks of 4 KB: block b at 4 KB * b = [dims 0..63: 16 rows x 128 B]
@@ -49,20 +31,7 @@ constexpr int kTileBytes = 2 * kHalfBytes;    // one 128 x 128 operand = 32 KB
 // A K tile holds the same bytes as [dims 0..63: block 0..7 x 16 rows][dims 64..127: ...]
 // (two 2-D boxes of 2 KB per block).
 constexpr int kBlockBytes = kBS * kD * 2;
-constexpr int kKStages = 3;                   // K tiles in flight (released when their S product is done)
-constexpr int kVStages = 3;                   // V tiles in flight (released when their PV product is done)
-constexpr int kSBufs = 3;                     // TMEM S/P buffers (128 columns each; O takes the 4th)
-// Q, K stages, V stages: 224 KB, which with the static barriers fills the 227 KB a CTA may
-// use, so the dynamic region carries no alignment slack; the kernel checks that it starts on
-// a 1 KB boundary (required by the 128-byte swizzle) and reports an error otherwise.
-constexpr int kSmemBytes = (1 + kKStages + kVStages) * kTileBytes;
 constexpr float kRescaleThreshold = 8.f;      // log2 units
-// A cluster is kCluster consecutive query tiles of one head and chunk.  They read the same K/V
-// tiles, so each CTA fetches a quarter of every tile's boxes and multicasts them to all: the
-// per-SM TMA work per tile drops by kCluster (one SM's TMA unit, not HBM or L2, bounds a
-// CTA that fetches all sixteen 4 KB boxes of a K+V tile itself).
-constexpr int kCluster = 4;
-constexpr uint16_t kClusterMask = (1u << kCluster) - 1;
 
 struct PrefillParams {
   void* out;
@@ -121,440 +90,30 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
-template <bool kBF16>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_k_full[kKStages], bar_k_empty[kKStages], bar_v_full[kVStages],
-      bar_v_empty[kVStages], bar_s_full[kSBufs], bar_p_full[kSBufs], bar_pv_done[kSBufs];
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ float row_xchg[2][2][kTile];                    // [use parity][half][row]: values the softmax halves swap
-  __shared__ __align__(8) uint64_t bar_xchg[2];              // 256 arrivals: both halves have written
-
-  const int qt = blockIdx.x, hq = blockIdx.y, c = blockIdx.z;
-  const int q0 = p.cu_q_lens[c];
-  const int qlen = p.cu_q_lens[c + 1] - q0;
-  const int r0 = qt * kTile;
-  // Decisions before the first cluster barrier must be the same for the whole cluster.
-  const int r0_cl = (qt & ~(kCluster - 1)) * kTile;           // first row of the cluster
-  if (qlen <= 0 || r0_cl >= qlen) return;                    // no rows for the whole cluster
-  const int start = p.q_start_pos[c];
-  const int ctx = start + qlen;                              // keys 0 .. ctx-1 exist
-  if (start < 0 || ctx > p.max_blocks * p.block_size) {
-    if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
-    return;
-  }
-  // Every CTA of the cluster walks the keys the cluster needs; a CTA whose rows end earlier
-  // finds the extra keys in its rows' future, where the causal mask zeroes them.  A CTA with
-  // no rows at all still takes part (its outputs are not stored).
-  const int kmax = start + min(qlen, r0_cl + kCluster * kTile);
-  const int nt = (kmax + kTile - 1) / kTile;
-  const uint32_t crank = cluster_ctarank();
-  const int G = p.num_heads / p.num_kv_heads;
-  const int h = hq / G;
-  const int nb = (ctx + kBS - 1) / kBS;
-  const int32_t* table = p.block_tables + int64_t(c) * p.max_blocks;
-
-  uint8_t* smem = smem_raw;
-  if (smem_u32(smem) & 1023u) {                              // see kSmemBytes
-    if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
-    return;
-  }
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTileBytes;                           // kKStages stages
-  uint8_t* sV = smem + (1 + kKStages) * kTileBytes;          // kVStages stages
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    prefetch_tensormap(&tmq);
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
-    mbar_init(&bar_q, 1);
-    // A stage is free again once every CTA of the cluster has released it.
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(&bar_k_full[i], 1);
-      mbar_init(&bar_k_empty[i], kCluster);
-    }
-    for (int i = 0; i < kVStages; ++i) {
-      mbar_init(&bar_v_full[i], 1);
-      mbar_init(&bar_v_empty[i], kCluster);
-    }
-    // The softmax warps signal P and the row-value swaps once per warp (lane 0, after the
-    // warp's own accesses): 8 arrivals a phase.
-    for (int i = 0; i < kSBufs; ++i) {
-      mbar_init(&bar_s_full[i], 1);
-      mbar_init(&bar_p_full[i], 8);
-    }
-    mbar_init(&bar_xchg[0], 8);
-    mbar_init(&bar_xchg[1], 8);
-    // PV_t's completion arrives on bar_pv_done[t % kSBufs].  A waiter for PV_t is always at most
-    // one phase behind that barrier (PV_{t+kSBufs} needs P_{t+kSBufs}, which the softmax has not
-    // produced yet), so waiting by phase parity is exact.  One barrier for every PV would not
-    // be: the softmax checks it only now and then, and the barrier can run two phases ahead.
-    for (int i = 0; i < kSBufs; ++i) mbar_init(&bar_pv_done[i], 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();                                            // every peer's barriers are initialised
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
-  const uint32_t tO = tmem + 128 * kSBufs;
-  auto tS = [&](int j) -> uint32_t { return tmem + 128 * uint32_t(j % kSBufs); };   // S_j, then P_j
-
-  if (warp == 0) {
-    // ---------------- TMA producer (the whole warp; lane 0 issues) ----------------
-    const uint64_t pol_q = l2_policy_evict_first();
-    const uint64_t pol_kv = l2_policy_evict_last();          // re-read by the other query heads
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar_q, kTileBytes);
-      tma_load_3d(sQ, &tmq, &bar_q, 0, hq, q0 + r0, pol_q);
-      tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq, q0 + r0, pol_q);
-    }
-    // Pool rows of the sequence's 16-row units, 32 per window (4 tiles): lane i holds unit
-    // 32 * w + i, which is block unit >> tile_shift at row offset 16 * (unit & mask).  Units
-    // past the sequence map to block 0 (their rows are masked / zeroed).
-    auto load_window = [&](int w) -> int {
-      const int lb = 32 * w + lane;
-      int pb = 0;
-      if (lb < nb) {
-        pb = table[lb >> p.tile_shift];
-        if (pb < 0 || pb >= p.num_blocks) {
-          set_error(p.err, PKV_DEVERR_BLOCK_ID);
-          pb = 0;
-        }
-      }
-      return (pb * p.num_kv_heads + h) * p.block_size + (lb & ((1 << p.tile_shift) - 1)) * kBS;
-    };
-    struct Window {
-      int cur, nxt, w;
-    };
-    // The window holding tile j (one ahead is always loaded, so the loads overlap the TMAs).
-    auto seek = [&](Window& win, int j) {
-      while (j / 4 > win.w) {
-        win.cur = win.nxt;
-        ++win.w;
-        win.nxt = load_window(win.w + 1);
-      }
-    };
-    Window wk{load_window(0), load_window(1), 0};
-    Window wv = wk;
-    // The 8 lanes that hold the tile's block rows issue its boxes that fall to this CTA
-    // (box % kCluster == rank), multicast to the whole cluster, in the same instruction.
-    // Each CTA's own full barrier expects the whole tile, most of it sent by its peers.
-    auto issue_k = [&](uint8_t* dst, uint64_t* bar, int j) {
-      seek(wk, j);
-      const int first = (8 * j) % 32;
-      if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
-      __syncwarp();
-      const int blk = lane - first;
-      if (blk >= 0 && blk < kTile / kBS) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          if (uint32_t((2 * blk + hf) % kCluster) == crank)
-            tma_load_3d_mc(dst + hf * kHalfBytes + blk * (kBlockBytes / 2), &tmk, bar, 0, wk.cur, hf, kClusterMask,
-                           pol_kv);
-        }
-      }
-    };
-    auto issue_v = [&](uint8_t* dst, uint64_t* bar, int j) {
-      seek(wv, j);
-      const int first = (8 * j) % 32;
-      if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
-      __syncwarp();
-      const int blk = lane - first;
-      if (blk >= 0 && blk < kTile / kBS && uint32_t(blk % kCluster) == crank)
-        tma_load_3d_mc(dst + blk * kBlockBytes, &tmv, bar, 0, wv.cur, 0, kClusterMask, pol_kv);
-    };
-    // K runs ahead of V; each is issued as soon as its stage has been released.  Lane 0
-    // polls the barriers and broadcasts, so the warp stays converged.
-    auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
-      uint32_t r = 0;
-      if (lane == 0) r = mbar_test(bar, parity) ? 1u : 0u;
-      return __shfl_sync(0xffffffffu, r, 0) != 0;
-    };
-    int kj = 0, vj = 0;
-    uint64_t t0 = 0;
-    bool ok = true;
-    while (ok && (kj < nt || vj < nt)) {
-      bool progress = false;
-      if (kj < nt && (kj < kKStages || ready(&bar_k_empty[kj % kKStages], uint32_t((kj - kKStages) / kKStages) & 1u))) {
-        issue_k(sK + (kj % kKStages) * kTileBytes, &bar_k_full[kj % kKStages], kj);
-        ++kj;
-        progress = true;
-      }
-      if (vj < kj && (vj < kVStages || ready(&bar_v_empty[vj % kVStages], uint32_t((vj - kVStages) / kVStages) & 1u))) {
-        issue_v(sV + (vj % kVStages) * kTileBytes, &bar_v_full[vj % kVStages], vj);
-        ++vj;
-        progress = true;
-      }
-      // Lane 0 keeps the clock, so every lane takes the same decision.  Idle polls back off
-      // so they do not take issue slots from the softmax warps on the same SM sub-partition.
-      if (!progress) __nanosleep(100);
-      uint32_t give_up = 0;
-      if (lane == 0) {
-        if (progress) {
-          t0 = 0;
-        } else if (t0 == 0) {
-          t0 = global_timer_ns();
-        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-          set_error(p.err, PKV_DEVERR_TIMEOUT);
-          give_up = 1;
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, give_up, 0) == 0;
-    }
-    // Drain: the last load of each stage must have landed, and every peer's release of the
-    // last tiles must have reached this CTA's barriers, before the CTA may leave the cluster.
-    if (lane == 0) {
-      for (int j = kj - kKStages < 0 ? 0 : kj - kKStages; j < kj; ++j)
-        (void)mbar_wait(&bar_k_full[j % kKStages], uint32_t(j / kKStages) & 1u);
-      for (int j = vj - kVStages < 0 ? 0 : vj - kVStages; j < vj; ++j)
-        (void)mbar_wait(&bar_v_full[j % kVStages], uint32_t(j / kVStages) & 1u);
-      for (int j = kj - kKStages < 0 ? 0 : kj - kKStages; j < kj; ++j)
-        (void)mbar_wait(&bar_k_empty[j % kKStages], uint32_t(j / kKStages) & 1u);
-      for (int j = vj - kVStages < 0 ? 0 : vj - kVStages; j < vj; ++j)
-        (void)mbar_wait(&bar_v_empty[j % kVStages], uint32_t(j / kVStages) & 1u);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    // S_j needs K_j and a free S buffer (PV_{j-2}, which reads P_{j-2} from that buffer,
-    // issued: tcgen05 ops of one thread execute in order); PV_j needs P_j and V_j.  Whichever
-    // is ready is issued first.
-    const uint32_t idesc_s = umma_idesc_f16(kBF16, 128, 128, false, false);
-    const uint32_t idesc_o = umma_idesc_f16(kBF16, 128, 128, false, true);
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-    bool ok = mbar_wait(&bar_q, 0);
-    int js = 0, jp = 0;
-    uint64_t t0 = 0;
-    while (ok && jp < nt) {
-      bool progress = false;
-      if (js < nt && js - jp < kSBufs && mbar_test(&bar_k_full[js % kKStages], uint32_t(js / kKStages) & 1u)) {
-        tc_fence_after();
-        const int st = js % kKStages;
-        const uint32_t tSj = tS(js);
-        // k-step kk: dims 16kk .. 16kk + 15 of Q and K, both stored as [64-dim half][rows]
-        // with 8-row groups 1 KB apart, so S column n is key n of the tile.
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_f16(tSj, umma_sdesc_sw128(aQ + off, 16, 1024), umma_sdesc_sw128(aK + st * kTileBytes + off, 16, 1024),
-                   idesc_s, kk > 0);
-        }
-        umma_commit(&bar_s_full[js % kSBufs]);
-        umma_commit_mc(&bar_k_empty[st], kClusterMask);     // released in every CTA of the cluster
-        ++js;
-        progress = true;
-      }
-      if (jp < js && mbar_test(&bar_p_full[jp % kSBufs], uint32_t(jp / kSBufs) & 1u) &&
-          mbar_test(&bar_v_full[jp % kVStages], uint32_t(jp / kVStages) & 1u)) {
-        tc_fence_after();
-        const int st = jp % kVStages;
-        // P_jp sits in the first 64 columns of its S buffer, two 16-bit values per column.
-        const uint32_t tP = tS(jp);
-        // k-step kk covers P columns 16kk .. 16kk + 15 = keys of block kk: its two 8-row
-        // groups sit 1 KB apart, its two 64-dim halves 2 KB apart.
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          umma_f16_ts(tO, tP + 8 * kk, umma_sdesc_sw128(aV + st * kTileBytes + kk * kBlockBytes, kBlockBytes / 2, 1024),
-                      idesc_o, jp > 0 || kk > 0);
-        }
-        umma_commit(&bar_pv_done[jp % kSBufs]);
-        umma_commit_mc(&bar_v_empty[st], kClusterMask);
-        ++jp;
-        progress = true;
-      }
-      if (progress) {
-        t0 = 0;
-      } else {
-        __nanosleep(50);
-        if (t0 == 0) {
-          t0 = global_timer_ns();
-        } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-          ok = false;
-        }
-      }
-    }
-    if (!ok) set_error(p.err, PKV_DEVERR_TIMEOUT);
-  } else if (warp >= 2) {
-    // ---------------- softmax: two warpgroups, one query row per thread in each ----------
-    // Warp w reaches TMEM lanes 32 * (w % 4) .. + 31, so warps 2..5 and 6..9 each cover all
-    // 128 rows; warpgroup `half` owns columns 64 * half .. + 63 of S, O and P.
-    const int half = (warp - 2) >> 2;
-    const int r = 32 * (warp & 3) + lane;                    // TMEM lane == row of the tile
-    const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-    const uint32_t col0 = 64 * half;
-    const int qrow = r0 + r;
-    const int pos = start + qrow;                            // absolute position of this query
-    const float sl = p.scale_log2;                           // > 0, so max(s) * sl = max(s * sl)
-    // Swap one float per row with the other half through shared memory; the k-th swap uses
-    // buffer and barrier k % 2 (bounded wait; the barrier's arrive/wait order the accesses).
-    int n_swaps = 0;
-    auto swap_halves = [&](float mine, float& theirs) -> bool {
-      const int b = n_swaps & 1;
-      row_xchg[b][half][r] = mine;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_xchg[b]);
-      const bool done = mbar_wait(&bar_xchg[b], uint32_t(n_swaps >> 1) & 1u);
-      theirs = row_xchg[b][half ^ 1][r];
-      ++n_swaps;
-      return done;
-    };
-    float m = -INFINITY, l = 0.f;                            // m in scaled log2 units
-    bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      if (!(ok = mbar_wait(&bar_s_full[j % kSBufs], uint32_t(j / kSBufs) & 1u))) break;
-      __syncwarp();
-      tc_fence_after();
-      float s[64];
-      {
-        float v[32];
-        const uint32_t tSj = tS(j) + lane_off + col0;
-        tmem_ld32(tSj, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = v[i];
-        tmem_ld32(tSj + 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
-      }
-      tmem_wait_ld();
-      // Column i of this half holds key kb + 64 * half + i.
-      const int lim = min(pos + 1, ctx) - (j * kTile + 64 * half);  // valid iff i < lim
-      float mraw = -INFINITY;
-      if (lim >= 64) {                                       // all 64 columns of this half valid
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, s[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          s[i] = i < lim ? s[i] : -INFINITY;
-          mraw = fmaxf(mraw, s[i]);
-        }
-      }
-      float other;
-      if (!(ok = swap_halves(mraw, other))) break;
-      const float mt = fmaxf(mraw, other) * sl;              // row max of the tile
-      const bool grow = mt > m + kRescaleThreshold;          // also true for the first tile
-      if (__any_sync(0xffffffffu, grow && j >= 1)) {
-        // O must be up to date (the previous PV product done) before it is rescaled.
-        if (!(ok = mbar_wait(&bar_pv_done[(j - 1) % kSBufs], uint32_t((j - 1) / kSBufs) & 1u))) break;
-        __syncwarp();
-        tc_fence_after();
-        const float alpha = (grow && m != -INFINITY) ? fast_exp2(m - mt) : 1.f;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float v[32];
-          tmem_ld32(tO + lane_off + col0 + 32 * cc, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tmem_st32(tO + lane_off + col0 + 32 * cc, v);
-        }
-        tmem_wait_st();
-        if (grow) l *= alpha;
-      }
-      if (grow) m = mt;
-      // The last key tile may reach past the sequence: zero those V rows so that 0 * garbage
-      // cannot turn into NaN inside the PV product.
-      const int kb = j * kTile;
-      if (kb + kTile > ctx) {
-        if (!(ok = mbar_wait(&bar_v_full[j % kVStages], uint32_t(j / kVStages) & 1u))) break;
-        if (kb + r >= ctx) {
-          const uint32_t vrow = smem_u32(sV + (j % kVStages) * kTileBytes) + (r / kBS) * kBlockBytes +
-                                half * (kBlockBytes / 2) + (r % kBS) * 128;
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) sts128(vrow + cc * 16, 0u, 0u, 0u, 0u);
-        }
-      }
-      // P = 2^(s * sl - m) as 16-bit pairs, written over this tile's S in TMEM: keys
-      // 64 * half .. + 63 go to columns 32 * half .. + 31 (the S values are in registers).
-      float lsum = 0.f;
-      uint32_t w[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float a = fast_exp2(fmaf(s[2 * e], sl, -m));
-        const float b = fast_exp2(fmaf(s[2 * e + 1], sl, -m));
-        lsum += a + b;
-        w[e] = pack_out<kBF16>(a, b);
-      }
-      tmem_st32u(tS(j) + lane_off + 32 * half, w);
-      tmem_wait_st();
-      l += lsum;
-      if (kb + kTile > ctx) fence_proxy_async_smem();        // the zeroed V rows, to the tensor cores
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p_full[j % kSBufs]);
-    }
-    if (ok) ok = mbar_wait(&bar_pv_done[(nt - 1) % kSBufs], uint32_t((nt - 1) / kSBufs) & 1u);
-    // Row sum = the two halves' partial sums (both used the same m).
-    if (ok) {
-      float other;
-      ok = swap_halves(l, other);
-      l += other;
-    }
-    __syncwarp();
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool live = qrow < qlen;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                            ((int64_t(q0) + qrow) * p.num_heads + hq) * (kD * 2) + col0 * 2);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        float v[32];
-        tmem_ld32(tO + lane_off + col0 + 32 * cc, v);
-        tmem_wait_ld();
-        if (live) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[cc * 4 + q4] = make_uint4(pack_out<kBF16>(v[8 * q4] * inv, v[8 * q4 + 1] * inv),
-                                          pack_out<kBF16>(v[8 * q4 + 2] * inv, v[8 * q4 + 3] * inv),
-                                          pack_out<kBF16>(v[8 * q4 + 4] * inv, v[8 * q4 + 5] * inv),
-                                          pack_out<kBF16>(v[8 * q4 + 6] * inv, v[8 * q4 + 7] * inv));
-        }
-      }
-    } else if (r == 0 && half == 0) {
-      set_error(p.err, PKV_DEVERR_TIMEOUT);
-    }
-    tc_fence_before();
-  }
-  __syncthreads();
-  cluster_sync();                                            // no peer sends to this CTA any more
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-
 // ---------------------------------------------------------------------------------------
-// Two query heads per CTA, the key range split in two, in clusters of four CTAs.
+// Two row blocks A and B of 128 query rows per CTA, the key range split between two CTAs.
 //
-// The query heads of a GQA group read the same K/V.  A CTA here takes two heads of one kv head
-// (128 rows each), so every K/V tile it receives feeds 256 query rows.  A cluster is two
-// adjacent q-tiles x two halves of their key range: the two CTAs of a half read the same keys,
-// each issues half of every tile's TMA boxes and multicasts them to both; the two halves of a
-// q-tile merge their partial results at the end.
-//   warp 0     : TMA producer: Q of both heads once, then its half of the boxes of K and V
-//                of the half's key tiles (2 stages each), multicast to the q-tile partner.  A
-//                stage is refilled once both CTAs' tensor-core commits have released it.
+// Rows that read the same K/V share a CTA, so every K/V tile it receives feeds 256 query rows:
+// - grouped heads (kQPair false): A and B are the same q-tile of two query heads of one kv head.
+//   A cluster is two adjacent q-tiles x two halves of their key range.  The two CTAs of a half
+//   read the same keys; each issues half of every tile's TMA boxes and multicasts them to both;
+// - one query head per kv head (kQPair true): A and B are two adjacent q-tiles of one head, and
+//   the cluster is the two halves of their key range; each CTA loads its tiles itself.
+// Both row blocks walk the keys the later rows need; the causal mask drops the rest.
+//   warp 0     : TMA producer: Q of both row blocks once, then the boxes of K and V of the
+//                half's key tiles (2 stages each).  A stage is refilled once every CTA that
+//                reads it has released it with a tensor-core commit.
 //   warp 1     : TMEM owner (512 columns: S_A | S_B | O_A | O_B) and MMA issuer, in the
 //                fixed order S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ... so that
-//                one head's softmax overlaps the other head's products.
-//   warps 2-5  : softmax of head A, warps 6-9: head B; one query row per thread.  The row's
+//                one block's softmax overlaps the other block's products.
+//   warps 2-5  : softmax of block A, warps 6-9: block B; one query row per thread.  The row's
 //                128 scores are read from TMEM once; the max uses 3-input max, P = 2^(s*c - m)
 //                uses packed fp32x2 multiply-add and add; P goes over S in TMEM; O is rescaled
 //                only when the row max grows by more than 2^8.
-// At the end the first-half CTA of a q-tile finishes head A and the second-half CTA head B.
-// Each CTA stages the other head's unnormalised O rows and (max, sum) in its idle stages and
-// sends them to its peer with bulk shared-memory copies; the receiver combines the two parts
-// by log-sum-exp, stages the 16-bit rows in the idle Q area and writes them out coalesced.
+// At the end the first-half CTA finishes block A and the second-half CTA block B.  Each CTA
+// stages the other block's unnormalised O rows and (max, sum) in its idle stages and sends
+// them to its peer with bulk shared-memory copies; the receiver combines the two parts by
+// log-sum-exp, stages the 16-bit rows in the idle Q area and writes them out coalesced.
 // ---------------------------------------------------------------------------------------
 constexpr int kPairThreads = 320;
 constexpr int kPairKStages = 2;
@@ -614,7 +173,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kQPair>
 __global__ void __launch_bounds__(kPairThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
@@ -625,16 +184,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __shared__ uint32_t tmem_base_sh;
 
   const int qt = blockIdx.x, slot = blockIdx.y, c = blockIdx.z >> 1;
-  const uint32_t crank = cluster_ctarank();                 // (q-tile of the pair) + 2 * (key half)
-  const uint32_t khalf = crank >> 1;
-  const uint16_t mc_mask = uint16_t(3u << (2 * khalf));     // the two CTAs reading this half's keys
+  // Grouped heads: crank = (q-tile of the pair) + 2 * (key half).  Query-tile pairs: the
+  // cluster is the two key halves, crank = key half.
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t khalf = kQPair ? crank : crank >> 1;
+  const uint16_t mc_mask = uint16_t(3u << (2 * khalf));     // the two CTAs reading this half's keys (grouped heads)
   // Launched as a programmatic dependent: the CTA may start while the previous kernel runs,
   // and reads nothing that kernel may write before this point.
   griddep_wait();
   const int q0 = p.cu_q_lens[c];
   const int qlen = p.cu_q_lens[c + 1] - q0;
-  const int r0 = qt * kTile;
-  const int r0_pair = (qt & ~1) * kTile;
+  // First query row of each of the CTA's two row blocks ("heads" A and B): the same q-tile of
+  // two query heads, or two adjacent q-tiles of one head.
+  const int r0_pair = kQPair ? 2 * qt * kTile : (qt & ~1) * kTile;
+  const int r0a = kQPair ? r0_pair : qt * kTile;
+  const int r0b = kQPair ? r0_pair + kTile : qt * kTile;
   // Every decision before the first cluster barrier is the same for all CTAs of the cluster.
   if (qlen <= 0 || r0_pair >= qlen) return;
   const int start = p.q_start_pos[c];
@@ -651,10 +215,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int j0 = khalf ? mid : 0;                            // this CTA's key tiles j0 .. j0 + n - 1
   const int n = khalf ? nt - mid : mid;
   const int G = p.num_heads / p.num_kv_heads;
-  const int spg = (G + 1) / 2;                               // head pairs (slots) per kv head
-  const int h = slot / spg;
-  const int hq0 = h * G + 2 * (slot % spg);
-  const int hq1 = 2 * (slot % spg) + 1 < G ? hq0 + 1 : hq0;  // an odd group's last slot repeats a head
+  const int spg = kQPair ? 1 : (G + 1) / 2;                  // head pairs (slots) per kv head
+  const int h = slot / spg;                                  // kv head
+  const int hq0 = kQPair ? slot : h * G + 2 * (slot % spg);
+  // An odd group's last slot repeats a head (its second part is computed and dropped).
+  const int hq1 = kQPair ? slot : (2 * (slot % spg) + 1 < G ? hq0 + 1 : hq0);
+  const bool b_live = kQPair || hq1 != hq0;                  // row block B is output
   const int nb = (ctx + kBS - 1) / kBS;
   const int32_t* table = p.block_tables + int64_t(c) * p.max_blocks;
 
@@ -677,11 +243,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     // CTA's tensor-core commit arrives on the stage's empty barrier in both.
     for (int i = 0; i < kPairKStages; ++i) {
       mbar_init(&bar_k_full[i], 1);
-      mbar_init(&bar_k_empty[i], 2);
+      mbar_init(&bar_k_empty[i], kQPair ? 1 : 2);
     }
     for (int i = 0; i < kPairVStages; ++i) {
       mbar_init(&bar_v_full[i], 1);
-      mbar_init(&bar_v_empty[i], 2);
+      mbar_init(&bar_v_empty[i], kQPair ? 1 : 2);
     }
     // One phase per key tile each.  A head's softmax waits on its pv_done only for the
     // product of the previous tile, and the next product needs this tile's P first, so the
@@ -714,10 +280,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint64_t pol_kv = l2_policy_evict_last();          // re-read by the other query heads
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar_q, 2 * kTileBytes);
-      tma_load_3d(sQ, &tmq, &bar_q, 0, hq0, q0 + r0, pol_q);
-      tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq0, q0 + r0, pol_q);
-      tma_load_3d(sQ + kTileBytes, &tmq, &bar_q, 0, hq1, q0 + r0, pol_q);
-      tma_load_3d(sQ + kTileBytes + kHalfBytes, &tmq, &bar_q, 64, hq1, q0 + r0, pol_q);
+      tma_load_3d(sQ, &tmq, &bar_q, 0, hq0, q0 + r0a, pol_q);
+      tma_load_3d(sQ + kHalfBytes, &tmq, &bar_q, 64, hq0, q0 + r0a, pol_q);
+      tma_load_3d(sQ + kTileBytes, &tmq, &bar_q, 0, hq1, q0 + r0b, pol_q);
+      tma_load_3d(sQ + kTileBytes + kHalfBytes, &tmq, &bar_q, 64, hq1, q0 + r0b, pol_q);
     }
     // Pool rows of the sequence's 16-row units, 32 per window (4 tiles); units past the
     // sequence map to block 0 (their rows are masked / zeroed).
@@ -751,9 +317,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
       __syncwarp();
       const int blk = lane - first;
-      if (blk >= 0 && blk < kTile / kBS) {                   // this CTA's half: the 64-dim half hf
-        const int hf = int(crank & 1u);
-        tma_load_3d_mc(dst + hf * kHalfBytes + blk * (kBlockBytes / 2), &tmk, bar, 0, wk.cur, hf, mc_mask, pol_kv);
+      if (blk >= 0 && blk < kTile / kBS) {
+        if constexpr (kQPair) {                              // both 64-dim halves, this CTA alone
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(dst + hf * kHalfBytes + blk * (kBlockBytes / 2), &tmk, bar, 0, wk.cur, hf, pol_kv);
+        } else {                                             // this CTA's half hf, to both CTAs
+          const int hf = int(crank & 1u);
+          tma_load_3d_mc(dst + hf * kHalfBytes + blk * (kBlockBytes / 2), &tmk, bar, 0, wk.cur, hf, mc_mask, pol_kv);
+        }
       }
     };
     auto issue_v = [&](uint8_t* dst, uint64_t* bar, int j) {
@@ -762,8 +334,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (lane == first) mbar_arrive_expect_tx(bar, kTileBytes);
       __syncwarp();
       const int blk = lane - first;
-      if (blk >= 0 && blk < kTile / kBS && uint32_t(blk & 1) == (crank & 1u))   // every other block
-        tma_load_3d_mc(dst + blk * kBlockBytes, &tmv, bar, 0, wv.cur, 0, mc_mask, pol_kv);
+      if constexpr (kQPair) {
+        if (blk >= 0 && blk < kTile / kBS) tma_load_3d(dst + blk * kBlockBytes, &tmv, bar, 0, wv.cur, 0, pol_kv);
+      } else {
+        if (blk >= 0 && blk < kTile / kBS && uint32_t(blk & 1) == (crank & 1u))   // every other block, to both
+          tma_load_3d_mc(dst + blk * kBlockBytes, &tmv, bar, 0, wv.cur, 0, mc_mask, pol_kv);
+      }
     };
     // The empty barriers also collect the partner CTA's releases: acquire at cluster scope.
     auto ready = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -832,7 +408,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                  umma_sdesc_sw128(aK + st * kTileBytes + off, 16, 1024), idesc_s, kk > 0);
       }
       umma_commit(&bar_s_full[x]);
-      if (x == 1) umma_commit_mc(&bar_k_empty[st], mc_mask); // both heads have read K_t: release it in both CTAs
+      if (x == 1) {                                          // both row blocks have read K_t: release it
+        if constexpr (kQPair) umma_commit(&bar_k_empty[st]);
+        else umma_commit_mc(&bar_k_empty[st], mc_mask);      // in both CTAs that read it
+      }
       return true;
     };
     // O_x += P_x(t) V_t, P_x in the first 64 columns of S_x.
@@ -848,7 +427,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     t > 0 || kk > 0);
       }
       umma_commit(&bar_pv_done[x]);
-      if (x == 1) umma_commit_mc(&bar_v_empty[st], mc_mask); // both heads have read V_t: release it in both CTAs
+      if (x == 1) {                                          // both row blocks have read V_t: release it
+        if constexpr (kQPair) umma_commit(&bar_v_empty[st]);
+        else umma_commit_mc(&bar_v_empty[st], mc_mask);      // in both CTAs that read it
+      }
       return true;
     };
     if (ok && n > 0) ok = issue_s(0, 0) && issue_s(1, 0);
@@ -862,7 +444,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int x = (warp - 2) >> 2;                             // head of this warpgroup (softmax warps)
   const int r = 32 * (warp & 3) + lane;                      // TMEM lane == row of the tile
   const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-  const int qrow = r0 + r;
+  const int qrow = (x == 0 ? r0a : r0b) + r;
   float m = -INFINITY, l = 0.f;                              // m in scaled log2 units
   if (warp >= 2) {
     const int pos = start + qrow;                            // absolute position of this query
@@ -979,8 +561,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   float* yO = reinterpret_cast<float*>(sK + kXAreaBytes);    // staging area
   float* yM = yO + kTile * kXStride;
   float* yL = yM + kTile;
-  const uint32_t xpeer = cluster_ctarank() ^ 2u;             // the same q-tile's other key half
-  const int fin = int(cluster_ctarank() >> 1);               // the head this CTA finishes: its key half
+  const uint32_t xpeer = cluster_ctarank() ^ (kQPair ? 1u : 2u);   // the same rows' other key half
+  const int fin = int(kQPair ? cluster_ctarank() : cluster_ctarank() >> 1);   // the row block this CTA finishes
   tc_fence_before();
   __syncthreads();                                           // this CTA's loads and products are all done
   tc_fence_after();
@@ -1031,7 +613,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     __syncwarp();
     if (!got) {
       if (r == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
-    } else if (x == 0 || hq1 != hq0) {                       // the whole warp: tcgen05.ld is collective
+    } else if (x == 0 || b_live) {                           // the whole warp: tcgen05.ld is collective
       const float mp = xM[r], lp = xL[r];
       const bool have = n > 0 && m != -INFINITY;
       const float mo = have ? m : -INFINITY;
@@ -1069,10 +651,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll 4
       for (int k = 0; k < 16; ++k) {
         const int rr = rw + 2 * k + (lane >> 4);
+        const int orow = (x == 0 ? r0a : r0b) + rr;
         const uint4 val = lds128(smem_u32(sQ) + rr * kOStride + (lane & 15) * 16);
-        if (r0 + rr < qlen)
+        if (orow < qlen)
           reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                   ((int64_t(q0) + r0 + rr) * p.num_heads + hq) * (kD * 2))[lane & 15] = val;
+                                   ((int64_t(q0) + orow) * p.num_heads + hq) * (kD * 2))[lane & 15] = val;
       }
     }
   }
@@ -1146,22 +729,29 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.err = err;
 
+  // Two row blocks of 128 query rows per CTA, the key range split between two CTAs.  Grouped
+  // heads: two query heads of a kv head, clusters of 2 q-tiles x 2 key halves.  One query
+  // head per kv head: two adjacent q-tiles of a head, clusters of the 2 key halves.
   const int G = num_heads / cache->num_kv_heads;
-  if (G >= 2) {
-    // Two query heads of a kv head per CTA; clusters of 2 q-tiles x 2 halves of the key range.
+  {
+    const bool qpair = G == 1;
     const int spg = (G + 1) / 2;
-    if (int64_t(num_chunks) * 2 > 65535 || int64_t(cache->num_kv_heads) * spg > 65535) return PKV_ERR_UNSUPPORTED;
-    auto pk = q_dtype == PKV_BF16 ? prefill_pair_kernel<true> : prefill_pair_kernel<false>;
+    const int qtiles = (max_q_len + kTile - 1) / kTile;
+    const dim3 grid = qpair ? dim3((qtiles + 1) / 2, num_heads, num_chunks * 2)
+                            : dim3((qtiles + 1) & ~1, cache->num_kv_heads * spg, num_chunks * 2);
+    if (int64_t(num_chunks) * 2 > 65535 || grid.y > 65535) return PKV_ERR_UNSUPPORTED;
+    auto pk = qpair ? (q_dtype == PKV_BF16 ? prefill_pair_kernel<true, true> : prefill_pair_kernel<false, true>)
+                    : (q_dtype == PKV_BF16 ? prefill_pair_kernel<true, false> : prefill_pair_kernel<false, false>);
     if (cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) != cudaSuccess)
       return PKV_ERR_CUDA;
     cudaLaunchConfig_t pc = {};
-    pc.gridDim = dim3(((max_q_len + kTile - 1) / kTile + 1) & ~1, cache->num_kv_heads * spg, num_chunks * 2);
+    pc.gridDim = grid;
     pc.blockDim = dim3(kPairThreads);
     pc.dynamicSmemBytes = kPairSmemBytes;
     pc.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute pa[2];
     pa[0].id = cudaLaunchAttributeClusterDimension;
-    pa[0].val.clusterDim.x = 2;
+    pa[0].val.clusterDim.x = qpair ? 1 : 2;
     pa[0].val.clusterDim.y = 1;
     pa[0].val.clusterDim.z = 2;
     pa[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1170,23 +760,4 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
     pc.numAttrs = 2;
     return cudaLaunchKernelEx(&pc, pk, tq, tk, tv, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   }
-  auto kern = q_dtype == PKV_BF16 ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  // Query tiles rounded up to whole clusters; tiles past a chunk's rows only help fetch K/V.
-  const int qtiles = (max_q_len + kTile - 1) / kTile;
-  dim3 grid((qtiles + kCluster - 1) / kCluster * kCluster, num_heads, num_chunks);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, prm) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
