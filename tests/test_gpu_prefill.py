@@ -127,6 +127,14 @@ def test_random_chunks(seed):
     _check(_case(10 + seed, chunks, hq, hkv, dtype, nan_fill=True, bs=bs), rows_per_chunk=list(range(0, 300, 7)))
 
 
+@pytest.mark.parametrize("bs", [16, 32])
+def test_mha_pairs_of_query_tiles(bs):
+    # one query head per kv head: a CTA takes two adjacent q-tiles of a head.  Chunks of 3, 2
+    # and 3 q-tiles (the last pair's second tile lies past the chunk), ragged tails, prefixes
+    # not aligned to 16 or 128.
+    _check(_case(8, [(0, 300), (77, 129), (500, 257), (3, 1)], 4, 4, "bf16", nan_fill=True, bs=bs))
+
+
 def test_gqa7_long_prefix():
     _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
 
