@@ -255,9 +255,10 @@ PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype 
  *   block_tables  (device) int32 [num_chunks][max_blocks_per_seq]
  *   max_q_len     host upper bound of the chunks' lengths (sizes the grid)
  * Supported: f16/bf16 cache with the same q dtype, head_dim 128, block_size 16 or 32,
- * num_heads / num_kv_heads in 1..8.  Tensor cores (tcgen05, TMEM accumulators), K/V
- * tiles fetched by TMA straight from the physical blocks and multicast to the four CTAs
- * of a cluster that read the same keys.  q, k_cache and v_cache must be device memory of
+ * num_heads a multiple of num_kv_heads (any group size).  Tensor cores (tcgen05, TMEM
+ * accumulators), K/V tiles fetched by TMA straight from the physical blocks; with two or
+ * more query heads per kv head they are multicast to the two CTAs of a cluster that read
+ * the same keys.  q, k_cache and v_cache must be device memory of
  * the current GPU (checked with cudaPointerGetAttributes before anything is enqueued):
  * host, managed or another GPU's memory returns PKV_ERR_INVALID_ARG.
  */

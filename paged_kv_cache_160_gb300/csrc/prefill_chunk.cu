@@ -454,6 +454,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int t = 0; t < n; ++t) {
       const int j = j0 + t;
       if (!(ok = mbar_wait(&bar_s_full[x], uint32_t(t) & 1u))) break;
+      // Observe every phase of pv_done: PV(t-1) is done by now (S(t) was issued after it), and
+      // waiting for it on every tile keeps the barrier at most one phase ahead of this wait, so
+      // the parity waits here and after the loop cannot mistake a phase two behind for a
+      // completed one (completion arrivals on different barriers may land out of order).
+      if (t >= 1 && !(ok = mbar_wait(&bar_pv_done[x], uint32_t(t - 1) & 1u))) break;
       __syncwarp();
       tc_fence_after();
       const int lim = min(pos + 1, ctx) - j * kTile;         // keys 0 .. lim-1 of the tile are valid
@@ -518,11 +523,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint64_t acc = add_f32x2(acc0, acc1);
       const float lsum = lo_f32(acc) + hi_f32(acc);
       if (__any_sync(0xffffffffu, grow && t >= 1)) {
-        // A row whose max grew rescales O, once the previous PV product has landed in it (the
-        // S values are dead by now, so the rescale does not add to the loop's live registers).
-        if (!(ok = mbar_wait(&bar_pv_done[x], uint32_t(t - 1) & 1u))) break;
-        __syncwarp();
-        tc_fence_after();
+        // A row whose max grew rescales O, into which the previous PV product has landed
+        // (waited for at the top of the tile).
         const float alpha = (grow && m_prev != -INFINITY) ? fast_exp2(m_prev - m) : 1.f;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {

@@ -135,6 +135,26 @@ def test_mha_pairs_of_query_tiles(bs):
     _check(_case(8, [(0, 300), (77, 129), (500, 257), (3, 1)], 4, 4, "bf16", nan_fill=True, bs=bs))
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 2), (4, 4)])
+def test_multi_tile_chunks_repeat_exactly(hq, hkv):
+    """Several key tiles per CTA and both halves of the key range: every run gives the same
+    bits.  (The wait for the last PV product once read O while products were still landing,
+    by a few ulps, differently from run to run.)"""
+    c = _case(11, [(37, 200), (300, 129), (128, 256)], hq, hkv, "bf16")
+    first, err = _run(c)
+    assert err == 0
+    for _ in range(4):
+        again, err = _run(c)
+        assert err == 0
+        assert torch.equal(first, again)
+
+
+@pytest.mark.parametrize("hq,hkv", [(6, 2), (32, 2)])
+def test_group_sizes_3_and_16(hq, hkv):
+    # an odd group (its last head pair repeats a head) and a group wider than the decode's 8
+    _check(_case(9, [(100, 200), (0, 130)], hq, hkv, "bf16"))
+
+
 def test_gqa7_long_prefix():
     _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
 
