@@ -239,8 +239,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
     mbar_init(&bar_q, 1);
-    // A stage is free again once both CTAs reading this half's keys have released it: each
-    // CTA's tensor-core commit arrives on the stage's empty barrier in both.
+    // A stage is free again once every CTA reading it has released it: with grouped heads the
+    // two CTAs of this key half (each one's tensor-core commit arrives on the stage's empty
+    // barrier in both), with query-tile pairs this CTA alone.
     for (int i = 0; i < kPairKStages; ++i) {
       mbar_init(&bar_k_full[i], 1);
       mbar_init(&bar_k_empty[i], kQPair ? 1 : 2);
@@ -249,8 +250,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(&bar_v_full[i], 1);
       mbar_init(&bar_v_empty[i], kQPair ? 1 : 2);
     }
-    // One phase per key tile each.  A head's softmax waits on its pv_done only for the
-    // product of the previous tile, and the next product needs this tile's P first, so the
+    // One phase per key tile each.  A row block's softmax waits on its pv_done on every tile,
+    // for the previous tile's product, and the next product needs this tile's P first, so the
     // barrier is never two phases ahead of its waiter.
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_s_full[x], 1);
@@ -440,8 +441,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (!ok) set_error(p.err, PKV_DEVERR_TIMEOUT);
   }
 
-  // ---------------- softmax: warps 2-5 head A, 6-9 head B; one row per thread ----------------
-  const int x = (warp - 2) >> 2;                             // head of this warpgroup (softmax warps)
+  // ---------------- softmax: warps 2-5 row block A, 6-9 row block B; one row per thread ----------------
+  const int x = (warp - 2) >> 2;                             // row block of this warpgroup (softmax warps)
   const int r = 32 * (warp & 3) + lane;                      // TMEM lane == row of the tile
   const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
   const int qrow = (x == 0 ? r0a : r0b) + r;
@@ -698,6 +699,8 @@ extern "C" pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtyp
   if (!(scale > 0.f)) return PKV_ERR_INVALID_ARG;          // the softmax takes max(s) * scale
   if (int64_t(cache->num_blocks) * cache->num_kv_heads * cache->block_size >= (int64_t(1) << 31))
     return PKV_ERR_UNSUPPORTED;
+  // The kernel bounds a chunk's context by max_blocks_per_seq * block_size in 32-bit arithmetic.
+  if (int64_t(max_blocks_per_seq) * cache->block_size >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
   // The K/V tiles are multicast across the CTAs of a cluster, so q and both caches must be
   // device memory of the current GPU: host, managed or another GPU's memory is refused
   // before any tensor map is built.

@@ -75,6 +75,20 @@ def test_argument_checks_run_on_host_without_gpu():
     assert L.pkv_stream_tiles(16, 16, ctypes.byref(desc), None, 4, 16, None) == 1
     assert L.pkv_stream_tiles(16, 16, ctypes.byref(desc), 16, 4, None, None) == 1
     assert L.pkv_stream_tiles(16, 16, ctypes.byref(desc), 16, 0, 16, None) == 0
+    # prefill: (out, q, q_dtype, cu_q_lens, q_start_pos, num_chunks, total_q, max_q_len, num_heads,
+    #          k, v, desc, tables, max_blocks_per_seq, scale, stream)
+    assert L.pkv_paged_prefill_chunk(16, 16, 1, 16, 16, 1, 8, 8, 6, 16, 16, ctypes.byref(desc), 16, 8, 0.1,
+                                     None) == 1                               # bad GQA split
+    assert L.pkv_paged_prefill_chunk(16, 16, 1, 16, 16, 1, 8, 8, 8, 16, 16, ctypes.byref(d96), 16, 8, 0.1,
+                                     None) == 2                               # head_dim 96
+    assert L.pkv_paged_prefill_chunk(16, 16, 0, 16, 16, 1, 8, 8, 8, 16, 16, ctypes.byref(desc), 16, 8, 0.1,
+                                     None) == 2                               # f16 q over a bf16 cache
+    assert L.pkv_paged_prefill_chunk(16, 16, 1, 16, 16, 1, 8, 8, 8, 16, 16, ctypes.byref(desc), 16, 1 << 27, 0.1,
+                                     None) == 2                               # table width x block_size >= 2^31
+    assert L.pkv_paged_prefill_chunk(16, 16, 1, 16, 16, 1, 8, 8, 8, 16, 16, ctypes.byref(desc), 16, 8, 0.0,
+                                     None) == 1                               # scale must be positive
+    assert L.pkv_paged_prefill_chunk(16, 16, 1, 16, 16, 0, 0, 0, 8, 16, 16, ctypes.byref(desc), 16, 8, 0.1,
+                                     None) == 0                               # nothing to do
     # the bounded-wait diagnostic takes a limit in (0, 1 s]
     assert L.pkv_check_bounded_wait(0, None) == 1
     assert L.pkv_check_bounded_wait(2_000_000_000, None) == 1
