@@ -189,41 +189,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t crank = cluster_ctarank();
   const uint32_t khalf = kQPair ? crank : crank >> 1;
   const uint16_t mc_mask = uint16_t(3u << (2 * khalf));     // the two CTAs reading this half's keys (grouped heads)
-  // Launched as a programmatic dependent: the CTA may start while the previous kernel runs,
-  // and reads nothing that kernel may write before this point.
-  griddep_wait();
-  const int q0 = p.cu_q_lens[c];
-  const int qlen = p.cu_q_lens[c + 1] - q0;
-  // First query row of each of the CTA's two row blocks ("heads" A and B): the same q-tile of
-  // two query heads, or two adjacent q-tiles of one head.
-  const int r0_pair = kQPair ? 2 * qt * kTile : (qt & ~1) * kTile;
-  const int r0a = kQPair ? r0_pair : qt * kTile;
-  const int r0b = kQPair ? r0_pair + kTile : qt * kTile;
-  // Every decision before the first cluster barrier is the same for all CTAs of the cluster.
-  if (qlen <= 0 || r0_pair >= qlen) return;
-  const int start = p.q_start_pos[c];
-  const int ctx = start + qlen;                              // keys 0 .. ctx-1 exist
-  if (start < 0 || ctx > p.max_blocks * p.block_size) {
-    if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
-    return;
-  }
-  // Both q-tiles of the pair walk the keys the later one needs (the earlier one finds the
-  // extra keys in its rows' future, masked); a q-tile past the chunk still takes part.
-  const int kmax = start + min(qlen, r0_pair + 2 * kTile);
-  const int nt = (kmax + kTile - 1) / kTile;
-  const int mid = (nt + 1) / 2;
-  const int j0 = khalf ? mid : 0;                            // this CTA's key tiles j0 .. j0 + n - 1
-  const int n = khalf ? nt - mid : mid;
-  const int G = p.num_heads / p.num_kv_heads;
-  const int spg = kQPair ? 1 : (G + 1) / 2;                  // head pairs (slots) per kv head
-  const int h = slot / spg;                                  // kv head
-  const int hq0 = kQPair ? slot : h * G + 2 * (slot % spg);
-  // An odd group's last slot repeats a head (its second part is computed and dropped).
-  const int hq1 = kQPair ? slot : (2 * (slot % spg) + 1 < G ? hq0 + 1 : hq0);
-  const bool b_live = kQPair || hq1 != hq0;                  // row block B is output
-  const int nb = (ctx + kBS - 1) / kBS;
-  const int32_t* table = p.block_tables + int64_t(c) * p.max_blocks;
-
   uint8_t* smem = smem_raw;
   if (smem_u32(smem) & 1023u) {                              // the 128-byte swizzle needs 1 KB alignment
     if (threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
@@ -274,6 +239,51 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   cluster_sync();                                            // every CTA's barriers are initialised
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+
+  // Launched as a programmatic dependent: the CTA may start while the previous kernel runs.
+  // Everything above reads no input; nothing below runs before that kernel has finished.
+  griddep_wait();
+  const int q0 = p.cu_q_lens[c];
+  const int qlen = p.cu_q_lens[c + 1] - q0;
+  // First query row of each of the CTA's two row blocks ("heads" A and B): the same q-tile of
+  // two query heads, or two adjacent q-tiles of one head.
+  const int r0_pair = kQPair ? 2 * qt * kTile : (qt & ~1) * kTile;
+  const int r0a = kQPair ? r0_pair : qt * kTile;
+  const int r0b = kQPair ? r0_pair + kTile : qt * kTile;
+  const int start = p.q_start_pos[c];
+  const int ctx = start + qlen;                              // keys 0 .. ctx-1 exist
+  // Nothing to do, or a bad chunk: the same for every CTA of the cluster, and nothing has been
+  // started that another CTA waits for; give back the TMEM and leave.
+  const bool idle = qlen <= 0 || r0_pair >= qlen;
+  const bool bad = !idle && (start < 0 || ctx > p.max_blocks * p.block_size);
+  if (idle || bad) {
+    if (bad && threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
+  // Both q-tiles of the pair walk the keys the later one needs (the earlier one finds the
+  // extra keys in its rows' future, masked); a q-tile past the chunk still takes part.
+  const int kmax = start + min(qlen, r0_pair + 2 * kTile);
+  const int nt = (kmax + kTile - 1) / kTile;
+  const int mid = (nt + 1) / 2;
+  const int j0 = khalf ? mid : 0;                            // this CTA's key tiles j0 .. j0 + n - 1
+  const int n = khalf ? nt - mid : mid;
+  const int G = p.num_heads / p.num_kv_heads;
+  const int spg = kQPair ? 1 : (G + 1) / 2;                  // head pairs (slots) per kv head
+  const int h = slot / spg;                                  // kv head
+  const int hq0 = kQPair ? slot : h * G + 2 * (slot % spg);
+  // An odd group's last slot repeats a head (its second part is computed and dropped).
+  const int hq1 = kQPair ? slot : (2 * (slot % spg) + 1 < G ? hq0 + 1 : hq0);
+  const bool b_live = kQPair || hq1 != hq0;                  // row block B is output
+  const int nb = (ctx + kBS - 1) / kBS;
+  const int32_t* table = p.block_tables + int64_t(c) * p.max_blocks;
+
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
