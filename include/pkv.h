@@ -261,6 +261,10 @@ PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype 
  * the same keys.  q, k_cache and v_cache must be device memory of
  * the current GPU (checked with cudaPointerGetAttributes before anything is enqueued):
  * host, managed or another GPU's memory returns PKV_ERR_INVALID_ARG.
+ * Launch order: launched as a programmatic dependent of the previous kernel on `stream`.
+ * Only the kernel's own shared-memory and tensor-memory set-up runs before that kernel has
+ * completed; no argument is read and no memory touched earlier, so stream order holds as
+ * for a plain launch.
  */
 PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
                                    const int32_t* cu_q_lens, const int32_t* q_start_pos,
