@@ -253,7 +253,8 @@ PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype 
  *   cu_q_lens     (device) int32 [num_chunks + 1], cu_q_lens[0] = 0, cu_q_lens[num_chunks] = total_q
  *   q_start_pos   (device) int32 [num_chunks]
  *   block_tables  (device) int32 [num_chunks][max_blocks_per_seq]
- *   max_q_len     host upper bound of the chunks' lengths (sizes the grid)
+ *   max_q_len     host upper bound of the chunks' lengths (sizes the grid); a longer chunk
+ *                 sets PKV_DEVERR_CHUNK and its rows past max_q_len stay unwritten
  * Supported: f16/bf16 cache with the same q dtype, head_dim 128, block_size 16 or 32,
  * num_heads a multiple of num_kv_heads (any group size).  Tensor cores (tcgen05, TMEM
  * accumulators), K/V tiles fetched by TMA straight from the physical blocks; with two or

@@ -256,6 +256,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   // started that another CTA waits for; give back the TMEM and leave.
   const bool idle = qlen <= 0 || r0_pair >= qlen;
   const bool bad = !idle && (start < 0 || ctx > p.max_blocks * p.block_size);
+  // A chunk longer than the grid covers (max_q_len below its length) leaves rows unwritten.
+  if (qt == int(gridDim.x) - 1 && threadIdx.x == 0 && qlen > int(gridDim.x) * (kQPair ? 2 : 1) * kTile)
+    set_error(p.err, PKV_DEVERR_CHUNK);
   if (idle || bad) {
     if (bad && threadIdx.x == 0) set_error(p.err, PKV_DEVERR_CHUNK);
     tc_fence_before();

@@ -159,6 +159,23 @@ def test_gqa7_long_prefix():
     _check(_case(3, [(3584, 512)], 28, 4, "bf16"), rows_per_chunk=[0, 1, 63, 127, 128, 300, 511])
 
 
+def test_max_q_len_below_a_chunk_length_is_flagged():
+    """max_q_len sizes the grid; a chunk longer than it is reported, not silently cut."""
+    import paged_kv_cache_160_gb300 as pkv
+    from paged_kv_cache_160_gb300._binding import DEVERR
+    for hq, hkv in ((8, 2), (4, 4)):
+        c = _case(12, [(10, 300)], hq, hkv, "bf16")
+        dev = torch.device("cuda")
+        kc, vc = c["k"].to(dev), c["v"].to(dev)
+        out = torch.zeros_like(c["q"]).to(dev)
+        pkv.pkv_get_device_error()
+        pkv.pkv_paged_prefill_chunk(out, c["q"].to(dev), torch.tensor(c["cu"], dtype=torch.int32, device=dev),
+                                    torch.tensor(c["starts"], dtype=torch.int32, device=dev), 100, kc, vc,
+                                    pkv.cache_desc(kc), torch.tensor(c["tables"], dtype=torch.int32, device=dev),
+                                    1 / math.sqrt(128))
+        assert pkv.pkv_get_device_error() & DEVERR["chunk"]
+
+
 def test_nan_in_unused_rows_never_reaches_output():
     _check(_case(4, [(5, 40), (77, 100)], 4, 1, "bf16", nan_fill=True))
 
