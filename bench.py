@@ -23,8 +23,9 @@ The same line also reports, each timed the same way:
   workloads                    the decode call on the 13B MHA batch and the long-context
                                e4m3 batch;
   mixed_step                   the mixed chunked-prefill + decode step as one graph per step:
-                               kv_write of 640 tokens, the 512-row prefill chunk, paged_decode
-                               of 128 sequences, then copy_blocks of 64 pairs;
+                               kv_write of 640 tokens; the 512-row prefill chunk on one stream
+                               beside paged_decode of 128 sequences on another; then
+                               copy_blocks of 64 pairs (and the same calls in one stream);
   prefill_chunk, cache_ops, swap_blocks, host_step: single calls;
   cpu_baseline                 the float64 oracle on the host cores, one core and all cores.
 
@@ -689,10 +690,12 @@ def decode_call_measure(n, dev, l2, stream, peak, K, W):
 
 
 def mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak):
-    """The mixed chunked-prefill + decode step as one graph per step: kv_write of all 640 new
-    rows (128 decode tokens, 512 chunk rows), paged_prefill_chunk of the 512-row chunk at
-    positions 3584..4095, paged_decode of the 128 sequences (+ merge), then copy_blocks of the
-    64 shared-prefix pairs.  K steps in one graph, rotating pool copies."""
+    """The mixed chunked-prefill + decode step: kv_write of all 640 new rows (128 decode
+    tokens, 512 chunk rows); then paged_prefill_chunk of the 512-row chunk at positions
+    3584..4095 on this stream beside paged_decode of the 128 sequences (+ merge) on a second
+    one, joined; then copy_blocks of the 64 shared-prefix pairs.  The prefill is tensor-bound
+    and leaves SMs free, the decode is HBM-bound, and neither reads what the other writes.
+    K steps in one graph, rotating pool copies; the same steps in one stream are timed too."""
     import torch
     import paged_kv_cache_160_gb300 as pkv
     import synth
@@ -722,21 +725,33 @@ def mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak):
     ctab = torch.tensor([plan.chunk_table], dtype=torch.int32, device=dev)
     pairs = torch.tensor(plan.share_pairs, dtype=torch.int32, device=dev)
 
-    def step(k):
+    s2 = torch.cuda.Stream(dev)
+    written, attended = torch.cuda.Event(), torch.cuda.Event()
+
+    def step(k, fork=True):
         r = k % R
         pkv.pkv_kv_write(k_all, v_all, slots, kcs[r], vcs[r], descs[r], stream)
+        if fork:
+            written.record(stream)
+            s2.wait_event(written)
         pkv.pkv_paged_prefill_chunk(cout, cq, cu, st0, ch.q_len, kcs[r], vcs[r], descs[r], ctab, case.scale, stream)
-        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, 0, ws, stream)
+        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, 0, ws,
+                             s2 if fork else stream)
+        if fork:
+            attended.record(s2)
+            stream.wait_event(attended)
         pkv.pkv_copy_blocks(kcs[r], vcs[r], descs[r], pairs, stream)
 
     ms = graph_ms(stream, step, K, W)
+    ms_serial = graph_ms(stream, lambda k: step(k, fork=False), K, W)
     assert pkv.pkv_get_device_error(stream) == 0
     res = {"workload": "mixed chunked-prefill + decode step: 512-row causal chunk at 3584..4095 over its paged "
                        "prefix, 128 decode seqs with context_lens U[256,4096] (seed 1605), 28/4 heads, head_dim 128, "
                        "bf16; kv_write 640 rows, then prefill chunk and paged_decode, then copy_blocks 64 pairs",
-           "ms_per_step": round(ms, 5), "launches_per_step": 5,
-           "what": "one CUDA graph of K steps: pkv_kv_write, pkv_paged_prefill_chunk, pkv_paged_decode "
-                   "(decode + merge), pkv_copy_blocks",
+           "ms_per_step": round(ms, 5), "serial_ms_per_step": round(ms_serial, 5), "launches_per_step": 5,
+           "what": "one CUDA graph of K steps: pkv_kv_write; pkv_paged_prefill_chunk on the bench stream "
+                   "beside pkv_paged_decode (decode + merge) on a second stream; pkv_copy_blocks after both. "
+                   "serial_ms_per_step: the same calls in one stream",
            "bytes_per_step": work["bytes"], "flops_per_step": work["flops"],
            "gbs": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
            "tflops": round(work["flops"] / (ms * 1e-3) / 1e12, 1),

@@ -1,0 +1,123 @@
+"""The mixed chunked-prefill step with its prefill chunk and its decodes on two streams.
+
+"Lecture 33 — KV Cache management", §4.2 batches a prefill chunk with the running decodes in
+one step.  The chunk's attention is tensor-bound and the decodes' attention is HBM-bound, so a
+serving loop runs them side by side: after kv_write, the prefill on one stream and the decode
+(+ merge) on another, joined before copy_blocks.  Neither call reads what the other writes, so
+the results must equal the serial order bit for bit, eagerly and as one captured graph.  The
+serial order itself is checked against the fp64 oracle by the parity tests.
+"""
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import paged_kv_cache_160_gb300  # noqa: F401  (fails loudly if the library is missing)
+
+
+def _setup():
+    import paged_kv_cache_160_gb300 as pkv
+    from paged_kv_cache_160_gb300.planner import product_plan
+    dev = torch.device("cuda")
+    case = synth.mixed_config()
+    plan = product_plan(case)
+    ch = case.chunk
+    s = {
+        "case": case, "plan": plan, "ch": ch,
+        "q": case.q.to(dev), "cq": ch.q.to(dev),
+        "k_all": torch.cat([case.k_new, ch.k_new]).to(dev),
+        "v_all": torch.cat([case.v_new, ch.v_new]).to(dev),
+        "slots": torch.tensor(list(plan.slots) + list(plan.chunk_slots), dtype=torch.int64, device=dev),
+        "tables": torch.tensor(plan.tables, dtype=torch.int32, device=dev),
+        "lens": torch.tensor(plan.lens, dtype=torch.int32, device=dev),
+        "max_len": max(plan.lens),
+        "cu": torch.tensor([0, ch.q_len], dtype=torch.int32, device=dev),
+        "st0": torch.tensor([ch.prefix_len], dtype=torch.int32, device=dev),
+        "ctab": torch.tensor([plan.chunk_table], dtype=torch.int32, device=dev),
+        "pairs": torch.tensor(plan.share_pairs, dtype=torch.int32, device=dev),
+    }
+    s["ws"] = torch.zeros(pkv.pkv_decode_workspace_bytes(case.num_seqs, case.num_heads, case.num_kv_heads,
+                                                         case.head_dim, case.block_size, s["max_len"], 0),
+                          dtype=torch.uint8, device=dev)
+    return s
+
+
+def _fresh(s):
+    """A pool copy, its descriptor and NaN-filled outputs."""
+    import paged_kv_cache_160_gb300 as pkv
+    dev = torch.device("cuda")
+    kc, vc = s["case"].k_cache.to(dev), s["case"].v_cache.to(dev)
+    return {"kc": kc, "vc": vc, "desc": pkv.cache_desc(kc),
+            "out": torch.full_like(s["q"], float("nan")), "cout": torch.full_like(s["cq"], float("nan"))}
+
+
+def _step(s, p, stream, s2=None, events=None):
+    """kv_write -> prefill chunk and paged_decode -> copy_blocks; on two streams when s2 is given."""
+    import paged_kv_cache_160_gb300 as pkv
+    case, ch = s["case"], s["ch"]
+    pkv.pkv_kv_write(s["k_all"], s["v_all"], s["slots"], p["kc"], p["vc"], p["desc"], stream)
+    dstream = stream
+    if s2 is not None:
+        events[0].record(stream)
+        s2.wait_event(events[0])
+        dstream = s2
+    pkv.pkv_paged_prefill_chunk(p["cout"], s["cq"], s["cu"], s["st0"], ch.q_len, p["kc"], p["vc"], p["desc"],
+                                s["ctab"], case.scale, stream)
+    pkv.pkv_paged_decode(p["out"], s["q"], p["kc"], p["vc"], p["desc"], s["tables"], s["lens"], s["max_len"],
+                         case.scale, 0, s["ws"], dstream)
+    if s2 is not None:
+        events[1].record(s2)
+        stream.wait_event(events[1])
+    pkv.pkv_copy_blocks(p["kc"], p["vc"], p["desc"], s["pairs"], stream)
+
+
+def _same(a, b):
+    for key in ("out", "cout", "kc", "vc"):
+        assert torch.equal(a[key].view(torch.uint8), b[key].view(torch.uint8)), key
+
+
+def test_two_streams_equal_the_serial_order_bit_for_bit():
+    import paged_kv_cache_160_gb300 as pkv
+    s = _setup()
+    stream, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    events = (torch.cuda.Event(), torch.cuda.Event())
+    serial, forked = _fresh(s), _fresh(s)
+    with torch.cuda.stream(stream):
+        _step(s, serial, stream)
+        _step(s, forked, stream, s2, events)
+    stream.synchronize()
+    assert pkv.pkv_get_device_error(stream) == 0
+    assert not torch.isnan(serial["out"]).any() and not torch.isnan(serial["cout"]).any()
+    _same(serial, forked)
+
+
+def test_two_streams_captured_as_one_graph():
+    """Two steps of the fork/join schedule captured in one CUDA graph and replayed twice."""
+    import paged_kv_cache_160_gb300 as pkv
+    s = _setup()
+    stream, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    events = (torch.cuda.Event(), torch.cuda.Event())
+    serial, graphed = _fresh(s), _fresh(s)
+    with torch.cuda.stream(stream):
+        _step(s, serial, stream)
+        _step(s, graphed, stream, s2, events)          # eager first: the library's device state exists
+    stream.synchronize()
+    graphed["out"].fill_(float("nan"))
+    graphed["cout"].fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for _ in range(2):
+            _step(s, graphed, stream, s2, events)
+    with torch.cuda.stream(stream):
+        g.replay()
+        g.replay()
+    stream.synchronize()
+    assert pkv.pkv_get_device_error(stream) == 0
+    _same(serial, graphed)
