@@ -23,9 +23,9 @@ The same line also reports, each timed the same way:
   workloads                    the decode call on the 13B MHA batch and the long-context
                                e4m3 batch;
   mixed_step                   the mixed chunked-prefill + decode step as one graph per step:
-                               kv_write of 640 tokens; the 512-row prefill chunk on one stream
-                               beside paged_decode of 128 sequences on another; then
-                               copy_blocks of 64 pairs (and the same calls in one stream);
+                               the 128 decodes (fused append, on 64 SMs) beside the 512 chunk
+                               rows' kv_write and prefill on another stream, then copy_blocks
+                               of 64 pairs (and the same work in one stream on every SM);
   prefill_chunk, cache_ops, swap_blocks, host_step: single calls;
   cpu_baseline                 the float64 oracle on the host cores, one core and all cores.
 
@@ -74,11 +74,11 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM bytes per decode call on the headline workload (paged_decode_kernel +
-# split_kv_merge_kernel, dram__bytes_read.sum + dram__bytes_write.sum, mean of the two calls
-# of one ncu capture; ncu flushes the caches before each kernel, so the merge's reads of the
+# split_kv_merge_kernel, dram__bytes_read.sum + dram__bytes_write.sum of one call in one ncu
+# capture; ncu flushes the caches before each kernel, so the merge's reads of the
 # partials count as DRAM reads), valid only for the kernel source with this hash; when the
 # source changes, traffic is reported as null until re-measured.
-TRAFFIC = {"source_sha1": "73262279ae0bdc2ea11a6170a31e3b2a9fb552fc", "bytes_per_launch": 160154496}
+TRAFFIC = {"source_sha1": "99b29df5523fdb6f246d2e32cb6d75fc16dafa77", "bytes_per_launch": 161419264}
 
 
 def _src_hash() -> str:
@@ -208,6 +208,13 @@ def prefill_work(case, plan):
     rows = ch.prefix_len + ch.q_len
     nbytes = 2 * rows * Hkv * D * 2 + 2 * ch.q_len * Hq * D * 2 + 4 * len(plan.chunk_table)
     return flops, nbytes
+
+
+# SMs the mixed step's decodes run on, beside the prefill chunk on the others.  Measured on
+# this step (decodes alone / the two-stream step, us): every SM 92 / 131; 88: 91 / 119;
+# 72: 93 / 110; 64: 100 / 107; 56: 112 / 116.  Below 72 SMs the decodes no longer saturate
+# HBM; above 64 the prefill's 128 CTAs get too few SMs.
+MIXED_DECODE_SMS = 64
 
 
 def mixed_step_work(case, plan):
@@ -690,19 +697,25 @@ def decode_call_measure(n, dev, l2, stream, peak, K, W):
 
 
 def mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak):
-    """The mixed chunked-prefill + decode step: kv_write of all 640 new rows (128 decode
-    tokens, 512 chunk rows); then paged_prefill_chunk of the 512-row chunk at positions
-    3584..4095 on this stream beside paged_decode of the 128 sequences (+ merge) on a second
-    one, joined; then copy_blocks of the 64 shared-prefix pairs.  The prefill is tensor-bound
-    and leaves SMs free, the decode is HBM-bound, and neither reads what the other writes.
-    K steps in one graph, rotating pool copies; the same steps in one stream are timed too."""
+    """The mixed chunked-prefill + decode step: 128 decode tokens and a 512-row chunk at
+    positions 3584..4095 (640 new rows), then copy_blocks of the 64 shared-prefix pairs.
+    The decodes are HBM-bound and the chunk's prefill tensor-bound, and neither reads what the
+    other writes, so they run side by side:
+    - this stream: pkv_paged_decode_append of the 128 sequences (their new rows written in the
+      same call) under an SM budget of MIXED_DECODE_SMS, then its merge;
+    - a second stream: pkv_kv_write of the chunk's 512 rows, then pkv_paged_prefill_chunk,
+      whose 128 CTAs take the other SMs;
+    - joined, then copy_blocks.
+    K steps in one graph, rotating pool copies.  serial_ms_per_step times the same work in one
+    stream on every SM: kv_write of the 640 rows, prefill, decode, copy_blocks."""
     import torch
     import paged_kv_cache_160_gb300 as pkv
     import synth
-    from paged_kv_cache_160_gb300.planner import product_plan
+    from paged_kv_cache_160_gb300.planner import append_slots, product_plan
     case = synth.mixed_config()
     plan = product_plan(case)
     assert not plan.cows, "the mixed step's decode tokens need no copy-on-write"
+    assert append_slots(case, plan) == list(plan.slots), "each decode token goes to its sequence's last position"
     work = mixed_step_work(case, plan)
     R = rotation(case, l2)
     kcs, vcs, descs = device_case(pkv, case, dev, R)
@@ -712,6 +725,9 @@ def mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak):
     k_all = torch.cat([case.k_new, ch.k_new]).to(dev)
     v_all = torch.cat([case.v_new, ch.v_new]).to(dev)
     slots = torch.tensor(list(plan.slots) + list(plan.chunk_slots), dtype=torch.int64, device=dev)
+    k_dec, v_dec = case.k_new.to(dev), case.v_new.to(dev)
+    k_ch, v_ch = ch.k_new.to(dev), ch.v_new.to(dev)
+    ch_slots = torch.tensor(list(plan.chunk_slots), dtype=torch.int64, device=dev)
     tables = torch.tensor(plan.tables, dtype=torch.int32, device=dev)
     lens = torch.tensor(plan.lens, dtype=torch.int32, device=dev)
     max_len = max(plan.lens)
@@ -726,32 +742,43 @@ def mixed_step_measure(dev, l2, stream, K, W, peak, bf16_peak):
     pairs = torch.tensor(plan.share_pairs, dtype=torch.int32, device=dev)
 
     s2 = torch.cuda.Stream(dev)
-    written, attended = torch.cuda.Event(), torch.cuda.Event()
+    forked, joined = torch.cuda.Event(), torch.cuda.Event()
 
-    def step(k, fork=True):
+    def split_step(k):
         r = k % R
-        pkv.pkv_kv_write(k_all, v_all, slots, kcs[r], vcs[r], descs[r], stream)
-        if fork:
-            written.record(stream)
-            s2.wait_event(written)
-        pkv.pkv_paged_prefill_chunk(cout, cq, cu, st0, ch.q_len, kcs[r], vcs[r], descs[r], ctab, case.scale, stream)
-        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, 0, ws,
-                             s2 if fork else stream)
-        if fork:
-            attended.record(s2)
-            stream.wait_event(attended)
+        forked.record(stream)
+        s2.wait_event(forked)                  # after the previous step's copy_blocks
+        pkv.pkv_paged_decode_append(out, q, k_dec, v_dec, kcs[r], vcs[r], descs[r], tables, lens, max_len,
+                                    case.scale, 0, ws, stream)
+        pkv.pkv_kv_write(k_ch, v_ch, ch_slots, kcs[r], vcs[r], descs[r], s2)
+        pkv.pkv_paged_prefill_chunk(cout, cq, cu, st0, ch.q_len, kcs[r], vcs[r], descs[r], ctab, case.scale, s2)
+        joined.record(s2)
+        stream.wait_event(joined)
         pkv.pkv_copy_blocks(kcs[r], vcs[r], descs[r], pairs, stream)
 
-    ms = graph_ms(stream, step, K, W)
-    ms_serial = graph_ms(stream, lambda k: step(k, fork=False), K, W)
+    def serial_step(k):
+        r = k % R
+        pkv.pkv_kv_write(k_all, v_all, slots, kcs[r], vcs[r], descs[r], stream)
+        pkv.pkv_paged_prefill_chunk(cout, cq, cu, st0, ch.q_len, kcs[r], vcs[r], descs[r], ctab, case.scale, stream)
+        pkv.pkv_paged_decode(out, q, kcs[r], vcs[r], descs[r], tables, lens, max_len, case.scale, 0, ws, stream)
+        pkv.pkv_copy_blocks(kcs[r], vcs[r], descs[r], pairs, stream)
+
+    pkv.pkv_set_decode_sm_budget(MIXED_DECODE_SMS)
+    try:
+        ms = graph_ms(stream, split_step, K, W)   # the budget is fixed in the graph at capture
+    finally:
+        pkv.pkv_set_decode_sm_budget(0)
+    ms_serial = graph_ms(stream, serial_step, K, W)
     assert pkv.pkv_get_device_error(stream) == 0
     res = {"workload": "mixed chunked-prefill + decode step: 512-row causal chunk at 3584..4095 over its paged "
                        "prefix, 128 decode seqs with context_lens U[256,4096] (seed 1605), 28/4 heads, head_dim 128, "
                        "bf16; kv_write 640 rows, then prefill chunk and paged_decode, then copy_blocks 64 pairs",
            "ms_per_step": round(ms, 5), "serial_ms_per_step": round(ms_serial, 5), "launches_per_step": 5,
-           "what": "one CUDA graph of K steps: pkv_kv_write; pkv_paged_prefill_chunk on the bench stream "
-                   "beside pkv_paged_decode (decode + merge) on a second stream; pkv_copy_blocks after both. "
-                   "serial_ms_per_step: the same calls in one stream",
+           "decode_sm_budget": MIXED_DECODE_SMS,
+           "what": "one CUDA graph of K steps: pkv_paged_decode_append (decode + merge) under the SM budget on the "
+                   "bench stream, beside pkv_kv_write of the chunk rows then pkv_paged_prefill_chunk on a second "
+                   "stream; pkv_copy_blocks after both. serial_ms_per_step: kv_write, prefill, decode, copy_blocks "
+                   "in one stream on every SM",
            "bytes_per_step": work["bytes"], "flops_per_step": work["flops"],
            "gbs": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
            "tflops": round(work["flops"] / (ms * 1e-3) / 1e12, 1),

@@ -243,6 +243,25 @@ PKV_API pkv_status pkv_paged_decode_noalloc(void* out, const void* q, pkv_dtype 
                                             pkv_stream_t stream);
 
 /*
+ * SM budget of the decode calls (pkv_paged_decode, _append, _noalloc).  The decode runs one
+ * persistent CTA per SM.  A budget n in 1 .. (SM count - 1) launches n CTAs instead, splitting
+ * the same work over fewer worker warps and leaving the other SMs to a kernel that runs
+ * beside it on another stream.  The use case is a chunk's tensor-bound prefill beside the
+ * step's HBM-bound decodes (Lecture 33 §4.2 batches the two in one step).  Under a budget the
+ * merge kernel launches when the decode grid has finished, not while it runs, so that its
+ * waiting CTAs do not hold those SMs.
+ *   num_sms  0 (the default) or >= the SM count: every SM.  Negative: PKV_ERR_INVALID_ARG,
+ *            the budget is unchanged.
+ * Results stay within the decode tolerances for any budget.  The split over workers
+ * changes, so fp32 sums are rounded in another order, and outputs are not bit-identical
+ * across budgets.  The setting is process-wide and applies to decode calls made after it,
+ * on every device and thread.  A captured graph keeps the grid of the call it captured.
+ * pkv_decode_workspace_bytes does not depend on the budget: it always sizes for every SM.
+ */
+PKV_API pkv_status pkv_set_decode_sm_budget(int num_sms);
+PKV_API int pkv_get_decode_sm_budget(void);
+
+/*
  * paged_prefill_chunk: causal attention of prefill chunks over their paged history
  * (Lecture 33 §4.2: a chunk attends the earlier chunks' cached KV, masked causally).
  * Chunk c holds query rows cu_q_lens[c] .. cu_q_lens[c+1]-1; row r of the chunk is at

@@ -21,6 +21,8 @@ from ._binding import (  # noqa: F401
     pkv_paged_decode_append,
     pkv_paged_decode_noalloc,
     pkv_noalloc_scratch_bytes,
+    pkv_get_decode_sm_budget,
+    pkv_set_decode_sm_budget,
     pkv_paged_prefill_chunk,
     pkv_stream_tiles,
     pkv_swap_blocks,

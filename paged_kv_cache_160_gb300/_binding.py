@@ -70,6 +70,10 @@ def _load() -> ctypes.CDLL:
                                             c_int, c_void_p, c_size_t, c_void_p]
     lib.pkv_noalloc_scratch_bytes.restype = c_size_t
     lib.pkv_noalloc_scratch_bytes.argtypes = []
+    lib.pkv_set_decode_sm_budget.restype = S
+    lib.pkv_set_decode_sm_budget.argtypes = [c_int]
+    lib.pkv_get_decode_sm_budget.restype = c_int
+    lib.pkv_get_decode_sm_budget.argtypes = []
     lib.pkv_paged_decode_noalloc.restype = S
     lib.pkv_paged_decode_noalloc.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p,
                                              POINTER(CacheDesc), c_void_p, c_int, c_void_p, c_int, c_float, c_int,
@@ -278,6 +282,15 @@ def pkv_paged_decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Ten
 
 def pkv_noalloc_scratch_bytes() -> int:
     return int(lib.pkv_noalloc_scratch_bytes())
+
+
+def pkv_set_decode_sm_budget(num_sms: int) -> None:
+    """SMs (persistent CTAs) the decode calls made after this use; 0 = every SM."""
+    _check(lib.pkv_set_decode_sm_budget(int(num_sms)), "pkv_set_decode_sm_budget")
+
+
+def pkv_get_decode_sm_budget() -> int:
+    return int(lib.pkv_get_decode_sm_budget())
 
 
 def pkv_paged_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

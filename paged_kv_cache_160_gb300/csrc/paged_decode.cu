@@ -36,6 +36,7 @@
 //   * Fused append (pkv_paged_decode_append): the warp holding a segment's last tile also
 //     places the step's new K/V row there, in the staged tile and in the cache.
 #include <algorithm>
+#include <atomic>
 #include <utility>
 
 #include "pkv_device.cuh"
@@ -82,6 +83,7 @@ struct DecodeParams {
   int tile_shift;         // log2(block_size / 16)
   int part_blocks;        // tiles per partition; 0 = balanced split
   int num_workers;        // gridDim.x * worker warps per CTA
+  int defer_dependents;   // 1: the merge kernel launches when this grid completes, not at its start
   float scale_log2;       // softmax scale * log2(e)
   float2* ml;             // [slots][group] (running max in log2 units, sum of exponentials)
   float* po;              // [slots][group][D] unnormalised partial outputs
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const int w = blockIdx.x * kWarps + warp;
   if (w >= W) {                              // no tiles for this warp
     griddep_wait();
-    griddep_launch_dependents();
+    if (!p.defer_dependents) griddep_launch_dependents();
     zero_empty();
     return;
   }
@@ -374,7 +376,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   // the outputs and the workspace are touched only after the preceding kernel on the stream
   // (typically the KV write of this step) has finished.
   griddep_wait();
-  griddep_launch_dependents();
+  // The merge kernel may be launched now, so that its CTAs take the SMs this grid frees and
+  // work out their pieces while the last tiles stream.  Under an SM budget the SMs outside
+  // this grid belong to another kernel: the merge then waits for this grid to finish.
+  if (!p.defer_dependents) griddep_launch_dependents();
   if (lane == 0) {
 #pragma unroll
     for (int i = 0; i < kStages; ++i)
@@ -865,7 +870,14 @@ pkv_status launch(const DecodeParams& prm, const CUtensorMap& tk, const CUtensor
   return PKV_ERR_UNSUPPORTED;
 }
 
-int decode_grid() { return std::max(1, num_sms()); }
+// One persistent CTA per SM, or per SM of the budget set with pkv_set_decode_sm_budget.
+// The workspace is always sized for the whole device, so any budget fits it.
+std::atomic<int> g_sm_budget{0};
+int full_grid() { return std::max(1, num_sms()); }
+int decode_grid() {
+  const int n = full_grid(), b = g_sm_budget.load(std::memory_order_relaxed);
+  return b > 0 && b < n ? b : n;
+}
 
 }  // namespace
 }  // namespace pkv
@@ -879,10 +891,18 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int num_kv_heads,
       partition_size < 0 || partition_size % kBS)
     return 0;
   const int group = num_heads / num_kv_heads;
-  const int workers = decode_grid() * kMaxWarps;
+  const int workers = full_grid() * kMaxWarps;
   const int64_t slots = num_slots(workers);
   return layout(group, head_dim, slots).total;
 }
+
+pkv_status pkv_set_decode_sm_budget(int num_sms) {
+  if (num_sms < 0) return PKV_ERR_INVALID_ARG;
+  pkv::g_sm_budget.store(num_sms, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+int pkv_get_decode_sm_budget(void) { return pkv::g_sm_budget.load(std::memory_order_relaxed); }
 
 }  // extern "C"
 
@@ -921,7 +941,7 @@ pkv_status decode_check(const void* out, const void* q, pkv_dtype q_dtype, int n
   const int64_t max_len = std::min<int64_t>(int64_t(max_blocks_per_seq) * cache->block_size, max_context_len);
   if (int64_t(cache->num_kv_heads) * num_seqs * ((max_len + kBS - 1) / kBS) >= (int64_t(1) << 31))
     return PKV_ERR_UNSUPPORTED;
-  const int grid = decode_grid();
+  const int grid = full_grid();
   if (int64_t(grid) * kMaxWarps >= (int64_t(1) << 16)) return PKV_ERR_UNSUPPORTED;
   *need = layout(group, D, num_slots(grid * kMaxWarps)).total;
   return PKV_OK;
@@ -994,6 +1014,7 @@ pkv_status decode_impl(void* out, const void* q, pkv_dtype q_dtype, int num_seqs
   prm.v_new = v_new;
   prm.k_cache = const_cast<void*>(k_cache);
   prm.v_cache = const_cast<void*>(v_cache);
+  prm.defer_dependents = grid < full_grid() ? 1 : 0;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool qbf = q_dtype == PKV_BF16;

@@ -33,6 +33,26 @@ def test_status_strings_and_version():
     assert pkv.lib.pkv_version() >= 1
 
 
+def test_decode_sm_budget_setting():
+    """The decode SM budget is a host setting: 0 (every SM) by default, any n >= 0 is kept,
+    a negative value is refused and leaves the budget as it was."""
+    import paged_kv_cache_160_gb300 as pkv
+    L = pkv.lib
+    assert L.pkv_get_decode_sm_budget() == 0
+    try:
+        assert L.pkv_set_decode_sm_budget(64) == 0
+        assert L.pkv_get_decode_sm_budget() == 64
+        assert L.pkv_set_decode_sm_budget(-1) == 1              # PKV_ERR_INVALID_ARG
+        assert L.pkv_get_decode_sm_budget() == 64
+        pkv.pkv_set_decode_sm_budget(100000)                    # clamped to the SM count at launch
+        assert pkv.pkv_get_decode_sm_budget() == 100000
+        with pytest.raises(pkv.PkvError):
+            pkv.pkv_set_decode_sm_budget(-5)
+    finally:
+        pkv.pkv_set_decode_sm_budget(0)
+    assert L.pkv_get_decode_sm_budget() == 0
+
+
 def test_argument_checks_run_on_host_without_gpu():
     import paged_kv_cache_160_gb300 as pkv
     from paged_kv_cache_160_gb300._binding import CacheDesc
