@@ -135,7 +135,7 @@ const char* pkv_status_string(pkv_status s) {
   return "unknown status";
 }
 
-int pkv_version(void) { return (0 << 16) | 1; }
+int pkv_version(void) { return (0 << 16) | 2; }
 
 pkv_status pkv_get_device_error(int* code, pkv_stream_t stream) {
   if (!code) return PKV_ERR_INVALID_ARG;
