@@ -93,3 +93,18 @@ def test_decode_tile_rows_follow_the_block_tables():
                 for j in range(0, L, 16):
                     want.append((t[j // bs] * 2 + h) * bs + j % bs)
         assert rows == want
+
+
+def test_mixed_step_decode_tokens_are_last_positions():
+    """The bench's mixed step writes its decode tokens inside pkv_paged_decode_append, which
+    stores each sequence's new row at position context_len - 1; that is the kv_write of the
+    serial step only if every decode token's slot is its sequence's last position.  The chunk
+    rows go through kv_write on the prefill's stream, and no slot is written twice."""
+    from paged_kv_cache_160_gb300.planner import append_slots
+    case = synth.mixed_config()
+    plan = product_plan(case)
+    assert not plan.cows
+    assert append_slots(case, plan) == list(plan.slots)
+    assert len(plan.slots) == case.num_seqs and len(plan.chunk_slots) == case.chunk.q_len
+    assert not set(plan.slots) & set(plan.chunk_slots)
+    assert bench.MIXED_DECODE_SMS > 0
