@@ -23,7 +23,7 @@ The same line also reports, each timed the same way:
   workloads                    the decode call on the 13B MHA batch and the long-context
                                e4m3 batch;
   mixed_step                   the mixed chunked-prefill + decode step as one graph per step:
-                               the 128 decodes (fused append, on 64 SMs) beside the 512 chunk
+                               the 128 decodes (fused append, on 66 SMs) beside the 512 chunk
                                rows' kv_write and prefill on another stream, then copy_blocks
                                of 64 pairs (and the same work in one stream on every SM);
   prefill_chunk, cache_ops, swap_blocks, host_step: single calls;
@@ -212,9 +212,10 @@ def prefill_work(case, plan):
 
 # SMs the mixed step's decodes run on, beside the prefill chunk on the others.  Measured on
 # this step (decodes alone / the two-stream step, us): every SM 92 / 131; 88: 91 / 119;
-# 72: 93 / 110; 64: 100 / 107; 56: 112 / 116.  Below 72 SMs the decodes no longer saturate
-# HBM; above 64 the prefill's 128 CTAs get too few SMs.
-MIXED_DECODE_SMS = 64
+# 72: 93 / 110; 64: 100 / 107; 56: 112 / 116; and the two-stream step alone at 60-70 SMs:
+# 60: 110; 62: 108-109; 64: 107; 66: 105.6; 68: 106-107; 70: 107.  Below 72 SMs the decodes
+# no longer saturate HBM; above about 66 the prefill's 128 CTAs get too few SMs.
+MIXED_DECODE_SMS = 66
 
 
 def mixed_step_work(case, plan):
