@@ -48,6 +48,12 @@ def test_decode_sm_budget_setting():
         assert pkv.pkv_get_decode_sm_budget() == 100000
         with pytest.raises(pkv.PkvError):
             pkv.pkv_set_decode_sm_budget(-5)
+        # the workspace is sized for every SM whatever the budget
+        args = (64, 28, 4, 128, 16, 2048, 0)
+        pkv.pkv_set_decode_sm_budget(0)
+        full = pkv.pkv_decode_workspace_bytes(*args)
+        pkv.pkv_set_decode_sm_budget(1)
+        assert pkv.pkv_decode_workspace_bytes(*args) == full > 0
     finally:
         pkv.pkv_set_decode_sm_budget(0)
     assert L.pkv_get_decode_sm_budget() == 0
